@@ -1,0 +1,286 @@
+/*
+ * fp8q.h -- C ABI of the scaled FP8 quantize -> FP8 GEMM library (libfp8q.so)
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (sources cited by page title and section):
+ *   [fp8_parity]  "fp8_parity.py", FP8 numerics lab (mlinterviewnotes.com):
+ *                 scaled_roundtrip, FP8Matmul, smoke steps 1-4.
+ *   [te_blog]     "How to Optimize Transformer-Based Models for Low-Precision
+ *                 Training" (repost of the NVIDIA blog): autocast vs
+ *                 pre-quantized GEMM timing, Fprop/Dgrad/Wgrad shapes,
+ *                 DelayedScaling with an amax history.
+ *   [sj_precision] SpikingJelly "Training and Inference Precision": FP8 Linear
+ *                 alignment (input dim % 16, output dim % 8), and "raises
+ *                 rather than falling back" when hardware or recipe is missing.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument that names tensor data is DEVICE memory owned by
+ *     the caller; the library never allocates, frees or retains it.  Host
+ *     pointers are only the small parameter structs (fp8q_operand) and the
+ *     optional host array of fp8q_history_init.
+ *   - Matrices are row-major and dense: element (r, c) of an [R, C] matrix is
+ *     at offset r * C + c.  bf16 is passed as raw 16-bit patterns.
+ *   - FP8 bytes: E4M3 (1-4-3, bias 7, no Inf, NaN = S.1111.111, max 448) and
+ *     E5M2 (1-5-2, bias 15, IEEE Inf/NaN, max 57344) ([fp8_parity] constants
+ *     E4M3_MAX / E5M2_MAX).
+ *   - Scales are fp32 DEQUANT multipliers: value = decode(byte) * s, and the
+ *     cast is byte = RNE_fp8(fl32(x / s)) with s = max(fl32(amax / fmax),
+ *     fl32(1e-12)) ([fp8_parity] scaled_roundtrip).  The quotient is the
+ *     correctly rounded fp32 division, as the definition states.
+ *   - saturate == 0: a quotient whose magnitude rounds above fmax becomes NaN
+ *     (E4M3) or Inf (E5M2), as a plain cast does ([fp8_parity] smoke step 2);
+ *     saturate != 0 clamps it to +-fmax.  NaN inputs stay NaN (0x7F | sign).
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream).  A
+ *     return of FP8Q_OK means the arguments were valid and the work was
+ *     enqueued.  Kernels that wait on hardware barriers give up after about a
+ *     second and record FP8Q_ERR_TIMEOUT in a device error word that
+ *     fp8q_device_status() reports after the stream completes.
+ *   - The library runs only on compute capability 10.3 (GB300).  Any other
+ *     device gives FP8Q_ERR_ARCH; there is no fallback path of any kind.
+ *   - Alignment: every device pointer must be 16-byte aligned
+ *     (FP8Q_ERR_MISALIGNED otherwise).  Inner (contiguous) dimensions must be
+ *     multiples of 16 where stated (FP8Q_ERR_INVALID_ARG otherwise).
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ codes */
+
+typedef enum fp8q_status {
+  FP8Q_OK = 0,
+  FP8Q_ERR_INVALID_ARG = 1,     /* null where required, negative size, bad enum,
+                                   inner dimension not a multiple of 16 */
+  FP8Q_ERR_MISALIGNED = 2,      /* a device pointer is not 16-byte aligned */
+  FP8Q_ERR_ARCH = 3,            /* current device is not compute capability 10.3 */
+  FP8Q_ERR_WORKSPACE = 4,       /* workspace missing or smaller than required */
+  FP8Q_ERR_TIMEOUT = 5,         /* a kernel's bounded wait expired (device-side) */
+  FP8Q_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed */
+  FP8Q_ERR_NOT_IMPLEMENTED = 7  /* valid request this build does not support */
+} fp8q_status;
+
+typedef enum fp8q_dtype {
+  FP8Q_DT_F32 = 0,
+  FP8Q_DT_BF16 = 1
+} fp8q_dtype;
+
+typedef enum fp8q_format {
+  FP8Q_E4M3 = 0,  /* activations and weights ([fp8_parity] FP8Matmul.forward) */
+  FP8Q_E5M2 = 1   /* output gradients ([fp8_parity] FP8Matmul.backward) */
+} fp8q_format;
+
+typedef enum fp8q_scaling {
+  FP8Q_SCALE_TENSOR = 0,      /* one scale for the whole operand */
+  FP8Q_SCALE_TILE_1x128 = 1,  /* one scale per row per 128-wide K block */
+  FP8Q_SCALE_BLOCK_128x128 = 2 /* one scale per 128x128 block */
+} fp8q_scaling;
+
+typedef enum fp8q_recipe {
+  FP8Q_RECIPE_TENSOR_CURRENT = 0, /* per-tensor, scale from this tensor's amax */
+  FP8Q_RECIPE_TENSOR_DELAYED = 1, /* per-tensor, scale from an amax history */
+  FP8Q_RECIPE_BLOCK = 2           /* 1x128 tiles on x, 128x128 blocks on w */
+} fp8q_recipe;
+
+/* Length of the delayed-scaling amax history ([fp8_parity] smoke step 3 keeps
+ * 16 past amaxes). */
+#define FP8Q_HISTORY_LEN 16
+
+/* Delayed-scaling state, in DEVICE memory, owned by the caller (80 bytes,
+ * 16-byte aligned).  It is plain data: copy it as raw bytes to checkpoint.
+ *   amax[]     the last FP8Q_HISTORY_LEN amax values (a ring)
+ *   next       index of the ring slot the next call overwrites
+ *   scale      the scale the most recent call used
+ *   pending, arrivals
+ *              zero between calls; used by a call in flight to combine the
+ *              per-block amax values.  Two calls on one state must not run
+ *              concurrently. */
+typedef struct fp8q_amax_history {
+  float amax[FP8Q_HISTORY_LEN];
+  int32_t next;
+  float scale;
+  uint32_t pending;
+  uint32_t arrivals;
+} fp8q_amax_history;
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Human-readable name of a status code (static storage). */
+const char *fp8q_status_string(int status);
+
+/* Reads and clears the device error word of the current device after
+ * synchronising the device.  Returns FP8Q_OK, FP8Q_ERR_TIMEOUT (a kernel's
+ * bounded barrier wait expired; its outputs are undefined) or FP8Q_ERR_CUDA. */
+int fp8q_device_status(void);
+
+/* 1 if the current device is compute capability 10.3, else 0. */
+int fp8q_device_supported(void);
+
+/* --------------------------------------------------------------- step a1 */
+
+/* amax = max |x| over n elements ([fp8_parity] scaled_roundtrip:
+ * x.abs().max()).  A NaN anywhere makes amax NaN; n == 0 gives 0.
+ *   x       device, n elements of in_dtype, 16-byte aligned
+ *   amax    device, one float, overwritten (the call first zeroes it on
+ *           `stream`)
+ * Errors: INVALID_ARG (null, n < 0, bad dtype), MISALIGNED, ARCH, CUDA. */
+int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax,
+             cudaStream_t stream);
+
+/* ----------------------------------------------------------- steps a2, a3 */
+
+/* Per-tensor current scaling ([fp8_parity] scaled_roundtrip with
+ * scale=None): s = max(fl32(*amax / fmax), 1e-12), q = RNE(x / s).
+ *   x          device [rows, cols] of in_dtype; cols % 16 == 0
+ *   amax       device float holding max|x| (from fp8_amax, or any value the
+ *              caller chooses: the cast uses it as given)
+ *   scale_out  device float or NULL: receives s
+ *   q          device [rows, cols] FP8 bytes or NULL
+ *   q_t        device [cols, rows] FP8 bytes (the transpose) or NULL;
+ *              requires rows % 16 == 0.  At least one of q, q_t non-NULL.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows,
+                        int64_t cols, int format, const float *amax,
+                        float *scale_out, uint8_t *q, uint8_t *q_t,
+                        int saturate, cudaStream_t stream);
+
+/* Per-tensor delayed scaling ([fp8_parity] smoke step 3; [te_blog]
+ * DelayedScaling "relies on an amax history"): s = max(fl32(max(hist->amax) /
+ * fmax), 1e-12) is computed from the history alone, x is cast with s, then
+ * amax(x) -- found in the same pass over x -- overwrites hist->amax[hist->next]
+ * and hist->next advances modulo FP8Q_HISTORY_LEN.  hist->scale receives s.
+ *   hist        device state (see fp8q_amax_history); exclusive to this call
+ *   scale_out, q, q_t, rows/cols rules as fp8_quantize_tensor
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_delayed(const void *x, int in_dtype, int64_t rows,
+                         int64_t cols, int format, fp8q_amax_history *hist,
+                         float *scale_out, uint8_t *q, uint8_t *q_t,
+                         int saturate, cudaStream_t stream);
+
+/* Writes a fresh history: amax[] from `initial` (HOST array of
+ * FP8Q_HISTORY_LEN floats) or zeros when NULL; next = 0, scale = 0, scratch
+ * words zero.  Synchronous with respect to the host. */
+int fp8q_history_init(fp8q_amax_history *hist, const float *initial,
+                      cudaStream_t stream);
+
+/* 1x128 tile scaling ([fp8_parity] smoke step 4 scales each 1x128 piece of a
+ * row on its own).  One read of x produces either or both of
+ *   row tiles:    q [rows, cols], q_scales [ceil(cols/128), rows] with
+ *                 scale(r, kb) = q_scales[kb * rows + r]  (tile = row r,
+ *                 columns [128 kb, 128 kb + 128))
+ *   column tiles: q_t [cols, rows] (the transpose), qt_scales
+ *                 [ceil(rows/128), cols] with scale(c, rb) =
+ *                 qt_scales[rb * cols + c] (tile = column c, rows
+ *                 [128 rb, 128 rb + 128)); i.e. 1x128 row tiles of x^T.
+ * Column tiles are what Wgrad needs: its contraction runs over x's rows.
+ * Partial edge tiles are allowed.  cols % 16 == 0; rows % 16 == 0 when the
+ * column-tile pair is requested.  Each pair is both-or-neither; at least one.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows,
+                           int64_t cols, int format, uint8_t *q,
+                           float *q_scales, uint8_t *q_t, float *qt_scales,
+                           int saturate, cudaStream_t stream);
+
+/* 128x128 block scaling for weights ([te_blog] "2D block scaling for
+ * weights"): one scale per block, block_scales [ceil(rows/128),
+ * ceil(cols/128)] row-major; q [rows, cols] and/or q_t [cols, rows] (the same
+ * bytes transposed -- a block's scale serves both orientations).
+ * cols % 16 == 0; rows % 16 == 0 when q_t is requested.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows,
+                              int64_t cols, int format, uint8_t *q,
+                              uint8_t *q_t, float *block_scales, int saturate,
+                              cudaStream_t stream);
+
+/* ----------------------------------------------------------- steps a4, a5 */
+
+/* One FP8 GEMM operand: `data` is a device [rows, K] row-major byte matrix
+ * (K contiguous, K % 16 == 0, 16-byte aligned).  The scale of element
+ * (row, k), kb = k / 128, is
+ *   FP8Q_SCALE_TENSOR:        scale[0]
+ *   FP8Q_SCALE_TILE_1x128:    scale[kb * scale_stride_k + row * scale_stride_row]
+ *   FP8Q_SCALE_BLOCK_128x128: scale[(row/128) * scale_stride_row + kb * scale_stride_k]
+ * (scale in device memory).  The quantize calls above produce:
+ *   tile scales of an [R, K] matrix:   stride_row = 1, stride_k = R
+ *   block scales of an [R, K] matrix:  stride_row = ceil(K/128), stride_k = 1
+ *   block scales used for the transpose [K, R]: stride_row = 1,
+ *                                      stride_k = ceil(K/128)  */
+typedef struct fp8q_operand {
+  const uint8_t *data;
+  int32_t format;
+  int32_t scaling;
+  const float *scale;
+  int64_t scale_stride_row;
+  int64_t scale_stride_k;
+} fp8q_operand;
+
+/* C[m, n] = sum_k A(m, k) * B(n, k) with each factor dequantised by its own
+ * scale, accumulated in fp32 on the tensor cores, then written as out_dtype
+ * (bf16, round-to-nearest-even, or fp32) to device C [M, N] row-major
+ * ([fp8_parity] FP8Matmul.forward: xq @ wq.T).  With TILE/BLOCK scaling the
+ * partial sum of every 128-wide K block is promoted into the fp32 result with
+ * that block's scale product.
+ *   A: [M, K], B: [N, K]; N % 16 == 0, K % 16 == 0; M >= 0 any.
+ *   M == 0 or N == 0: nothing to do.  K == 0: C is zero.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, NOT_IMPLEMENTED (a TILE/BLOCK
+ * combination outside: A TILE with B TILE or BLOCK), CUDA. */
+int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C,
+             int out_dtype, int64_t M, int64_t N, int64_t K,
+             cudaStream_t stream);
+
+/* The three GEMMs of a linear layer y = x w^T with x [M, K] (tokens x input
+ * features), w [N, K], grad_out g [M, N] ([fp8_parity] FP8Matmul; [te_blog]
+ * "Fprop, Dgrad, and Wgrad shapes are all benchmarked individually").  M, N, K
+ * are always the LAYER's sizes; each call maps them onto fp8_gemm:
+ *   fprop: y [M, N]  = x [M, K] . w [N, K]^T        (contraction K)
+ *   dgrad: dx [M, K] = g [M, N] . w                 (contraction N;
+ *          pass w_t = w^T as a [K, N] operand, e.g. q_t of the weight)
+ *   wgrad: dw [N, K] = g^T . x                      (contraction M;
+ *          pass g_t [N, M] and x_t [K, M], e.g. column-tile / q_t outputs)
+ * Alignment: the contraction and the output column count must be multiples
+ * of 16 (so M % 16 == 0 for wgrad).  Errors as fp8_gemm. */
+int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y,
+                   int out_dtype, int64_t M, int64_t N, int64_t K,
+                   cudaStream_t stream);
+int fp8_gemm_dgrad(const fp8q_operand *g, const fp8q_operand *w_t, void *dx,
+                   int out_dtype, int64_t M, int64_t N, int64_t K,
+                   cudaStream_t stream);
+int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw,
+                   int out_dtype, int64_t M, int64_t N, int64_t K,
+                   cudaStream_t stream);
+
+/* ----------------------------------------------------- the whole forward */
+
+/* Bytes of workspace fp8_linear_autocast needs for this recipe and shape
+ * (rounded up to 256-byte pieces). */
+size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K);
+
+/* Autocast forward of a linear layer ([te_blog] "autocast mode": inputs are
+ * quantized dynamically before each GEMM, and the time covers both): with
+ * x [M, K] and w [N, K] in in_dtype, quantizes both to E4M3 under `recipe`
+ * and computes y [M, N] = x w^T in out_dtype, all on `stream`, without
+ * synchronising.
+ *   TENSOR_CURRENT: amax(x), amax(w), cast x, cast w, per-tensor GEMM
+ *   TENSOR_DELAYED: casts with hist_x / hist_w (device state, required)
+ *   BLOCK:          1x128 row tiles of x, 128x128 blocks of w, promoted GEMM
+ *   workspace  device scratch of at least fp8q_linear_workspace_size bytes,
+ *              256-byte aligned; holds the FP8 copies, scales and amaxes
+ * Alignment: K % 16 == 0, N % 16 == 0.
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE, ARCH, CUDA. */
+int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M,
+                        int64_t N, int64_t K, int recipe,
+                        fp8q_amax_history *hist_x, fp8q_amax_history *hist_w,
+                        void *y, int out_dtype, void *workspace,
+                        size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8Q_H */

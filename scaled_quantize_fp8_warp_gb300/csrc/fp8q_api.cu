@@ -1,0 +1,426 @@
+// The extern "C" boundary of libfp8q.so (declared in include/fp8q.h):
+// argument validation, device checks, and dispatch to the kernels.  No entry
+// point allocates device memory; none synchronises except the diagnostics
+// and fp8q_history_init.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "fp8q_internal.h"
+
+namespace fp8q {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// Word set by kernels whose bounded waits expire.  One copy per device (the
+// module is loaded per context); its address is looked up per device.
+__device__ unsigned int g_error_word = 0;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int supported = 0;
+  int sms = 0;
+  unsigned int *err = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+DeviceInfo *current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo *d = &g_dev[dev];
+  std::call_once(d->once, [d, dev] {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return;
+    d->supported = (prop.major == 10 && prop.minor == 3) ? 1 : 0;
+    d->sms = prop.multiProcessorCount;
+    void *p = nullptr;
+    if (d->supported && cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess)
+      d->err = static_cast<unsigned int *>(p);
+  });
+  return d;
+}
+
+bool log_enabled() {
+  static int on = -1;
+  if (on < 0) {
+    const char *e = getenv("FP8Q_LOG");
+    on = (e != nullptr && e[0] != '\0' && e[0] != '0') ? 1 : 0;
+  }
+  return on == 1;
+}
+
+int check_device() {
+  DeviceInfo *d = current_device();
+  if (d == nullptr) return FP8Q_ERR_CUDA;
+  return d->supported ? FP8Q_OK : FP8Q_ERR_ARCH;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_dtype(int d) { return d == FP8Q_DT_F32 || d == FP8Q_DT_BF16; }
+bool valid_format(int f) { return f == FP8Q_E4M3 || f == FP8Q_E5M2; }
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA; }
+
+// Shared validation of the quantize calls.
+int check_quant(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                bool want_t) {
+  if (!valid_dtype(in_dtype) || !valid_format(format)) return FP8Q_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0) return FP8Q_ERR_INVALID_ARG;
+  if (cols % 16 != 0) return FP8Q_ERR_INVALID_ARG;
+  if (want_t && rows % 16 != 0) return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0) {
+    if (x == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(x)) return FP8Q_ERR_MISALIGNED;
+  }
+  return FP8Q_OK;
+}
+
+int check_ptr(const void *p, bool required) {
+  if (p == nullptr) return required ? FP8Q_ERR_INVALID_ARG : FP8Q_OK;
+  return aligned16(p) ? FP8Q_OK : FP8Q_ERR_MISALIGNED;
+}
+
+int check_operand(const fp8q_operand *op, int64_t rows, int64_t K) {
+  if (op == nullptr || !valid_format(op->format)) return FP8Q_ERR_INVALID_ARG;
+  if (op->scaling != FP8Q_SCALE_TENSOR && op->scaling != FP8Q_SCALE_TILE_1x128 &&
+      op->scaling != FP8Q_SCALE_BLOCK_128x128)
+    return FP8Q_ERR_INVALID_ARG;
+  if (op->scale == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(op->scale) & 3u) != 0) return FP8Q_ERR_MISALIGNED;
+  if (op->scaling != FP8Q_SCALE_TENSOR && (op->scale_stride_row < 0 || op->scale_stride_k < 0))
+    return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && K > 0) {
+    if (op->data == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(op->data)) return FP8Q_ERR_MISALIGNED;
+  }
+  return FP8Q_OK;
+}
+
+GemmOperandDev to_dev(const fp8q_operand *op) {
+  GemmOperandDev d;
+  d.data = op->data;
+  d.format = op->format;
+  d.scaling = op->scaling;
+  d.scale = op->scale;
+  d.stride_row = op->scale_stride_row;
+  d.stride_k = op->scale_stride_k;
+  return d;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+unsigned int *device_error_word() {
+  DeviceInfo *d = current_device();
+  return d ? d->err : nullptr;
+}
+
+int sm_count() {
+  DeviceInfo *d = current_device();
+  return (d && d->sms > 0) ? d->sms : kNumSMsHint;
+}
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" {
+
+const char *fp8q_status_string(int status) {
+  switch (status) {
+    case FP8Q_OK: return "ok";
+    case FP8Q_ERR_INVALID_ARG: return "invalid argument";
+    case FP8Q_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FP8Q_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case FP8Q_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8Q_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case FP8Q_ERR_CUDA: return "CUDA error";
+    case FP8Q_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+int fp8q_device_supported(void) { return check_device() == FP8Q_OK ? 1 : 0; }
+
+int fp8q_device_status(void) {
+  int rc = check_device();
+  if (rc != FP8Q_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FP8Q_ERR_CUDA;
+  unsigned int *w = device_error_word();
+  if (w == nullptr) return FP8Q_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (v != 0) {
+    unsigned int zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return FP8Q_ERR_CUDA;
+    return FP8Q_ERR_TIMEOUT;
+  }
+  return FP8Q_OK;
+}
+
+int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax, cudaStream_t stream) {
+  if (!valid_dtype(in_dtype) || n < 0 || amax == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (n > 0 && x == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (n > 0 && !aligned16(x)) return FP8Q_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(amax) & 3u) != 0) return FP8Q_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != FP8Q_OK) return rc;
+  return from_cuda(launch_amax(x, in_dtype, n, amax, stream));
+}
+
+int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                        const float *amax, float *scale_out, uint8_t *q, uint8_t *q_t,
+                        int saturate, cudaStream_t stream) {
+  int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
+  if (rc != FP8Q_OK) return rc;
+  if (amax == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.mode = kModeTensorCurrent;
+  p.amax_in = amax;
+  p.scale_out = scale_out;
+  p.q = q;
+  p.q_t = q_t;
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] quantize_tensor %lldx%lld fmt=%d q=%d q_t=%d\n", (long long)rows,
+            (long long)cols, format, q != nullptr, q_t != nullptr);
+  return from_cuda(launch_quant2d(p, stream));
+}
+
+int fp8_quantize_delayed(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                         fp8q_amax_history *hist, float *scale_out, uint8_t *q, uint8_t *q_t,
+                         int saturate, cudaStream_t stream) {
+  int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
+  if (rc != FP8Q_OK) return rc;
+  if (hist == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_ptr(hist, true)) != FP8Q_OK) return rc;
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.mode = kModeTensorDelayed;
+  p.hist = hist;
+  p.scale_out = scale_out;
+  p.q = q;
+  p.q_t = q_t;
+  return from_cuda(launch_quant2d(p, stream));
+}
+
+int fp8q_history_init(fp8q_amax_history *hist, const float *initial, cudaStream_t stream) {
+  if (hist == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (!aligned16(hist)) return FP8Q_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != FP8Q_OK) return rc;
+  fp8q_amax_history h{};
+  if (initial != nullptr)
+    for (int i = 0; i < FP8Q_HISTORY_LEN; ++i) h.amax[i] = initial[i];
+  if (cudaMemcpyAsync(hist, &h, sizeof h, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  return from_cuda(cudaStreamSynchronize(stream));
+}
+
+int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                           uint8_t *q, float *q_scales, uint8_t *q_t, float *qt_scales,
+                           int saturate, cudaStream_t stream) {
+  const bool want_row = q != nullptr || q_scales != nullptr;
+  const bool want_col = q_t != nullptr || qt_scales != nullptr;
+  int rc = check_quant(x, in_dtype, rows, cols, format, want_col);
+  if (rc != FP8Q_OK) return rc;
+  if (!want_row && !want_col) return FP8Q_ERR_INVALID_ARG;
+  if (want_row && (q == nullptr || q_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if (want_col && (q_t == nullptr || qt_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if ((q_scales && (reinterpret_cast<uintptr_t>(q_scales) & 3u)) ||
+      (qt_scales && (reinterpret_cast<uintptr_t>(qt_scales) & 3u)))
+    return FP8Q_ERR_MISALIGNED;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  if (rows == 0 || cols == 0) return FP8Q_OK;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.mode = kModeTile;
+  p.q = want_row ? q : nullptr;
+  p.q_scales = want_row ? q_scales : nullptr;
+  p.q_t = want_col ? q_t : nullptr;
+  p.qt_scales = want_col ? qt_scales : nullptr;
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] quantize_tile1x128 %lldx%lld fmt=%d rows=%d cols=%d\n",
+            (long long)rows, (long long)cols, format, want_row, want_col);
+  return from_cuda(launch_quant2d(p, stream));
+}
+
+int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t cols,
+                              int format, uint8_t *q, uint8_t *q_t, float *block_scales,
+                              int saturate, cudaStream_t stream) {
+  int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
+  if (rc != FP8Q_OK) return rc;
+  if (block_scales == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if (reinterpret_cast<uintptr_t>(block_scales) & 3u) return FP8Q_ERR_MISALIGNED;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  if (rows == 0 || cols == 0) return FP8Q_OK;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.mode = kModeBlock;
+  p.q = q;
+  p.q_t = q_t;
+  p.q_scales = block_scales;
+  return from_cuda(launch_quant2d(p, stream));
+}
+
+int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t M,
+             int64_t N, int64_t K, cudaStream_t stream) {
+  if (M < 0 || N < 0 || K < 0 || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
+  if (N % 16 != 0 || K % 16 != 0) return FP8Q_ERR_INVALID_ARG;
+  int rc;
+  if ((rc = check_operand(A, M, K)) != FP8Q_OK) return rc;
+  if ((rc = check_operand(B, N, K)) != FP8Q_OK) return rc;
+  if (M > 0 && N > 0) {
+    if (C == nullptr) return FP8Q_ERR_INVALID_ARG;
+    if (!aligned16(C)) return FP8Q_ERR_MISALIGNED;
+  }
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] gemm M=%lld N=%lld K=%lld A(fmt=%d,scale=%d) B(fmt=%d,scale=%d) out=%d\n",
+            (long long)M, (long long)N, (long long)K, A->format, A->scaling, B->format,
+            B->scaling, out_dtype);
+  return launch_gemm(to_dev(A), to_dev(B), C, out_dtype, M, N, K, stream);
+}
+
+int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y, int out_dtype,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  // y [M, N] = x [M, K] . w [N, K]^T
+  return fp8_gemm(x, w, y, out_dtype, M, N, K, stream);
+}
+
+int fp8_gemm_dgrad(const fp8q_operand *g, const fp8q_operand *w_t, void *dx, int out_dtype,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  // dx [M, K] = g [M, N] . (w_t [K, N])^T, contraction over N
+  return fp8_gemm(g, w_t, dx, out_dtype, M, K, N, stream);
+}
+
+int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw, int out_dtype,
+                   int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  // dw [N, K] = g_t [N, M] . (x_t [K, M])^T, contraction over M
+  return fp8_gemm(g_t, x_t, dw, out_dtype, N, K, M, stream);
+}
+
+size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  size_t b = round256((size_t)(M * K)) + round256((size_t)(N * K));  // FP8 copies of x, w
+  b += 2 * round256(sizeof(float)) * 2;                               // amax + scale for x, w
+  if (recipe == FP8Q_RECIPE_BLOCK) {
+    b += round256(sizeof(float) * (size_t)(((K + 127) / 128) * M));    // x tile scales
+    b += round256(sizeof(float) * (size_t)(((N + 127) / 128) * ((K + 127) / 128)));
+  }
+  return b;
+}
+
+int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M, int64_t N,
+                        int64_t K, int recipe, fp8q_amax_history *hist_x,
+                        fp8q_amax_history *hist_w, void *y, int out_dtype, void *workspace,
+                        size_t ws_bytes, cudaStream_t stream) {
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || K % 16 != 0 || N % 16 != 0) return FP8Q_ERR_INVALID_ARG;
+  if (recipe != FP8Q_RECIPE_TENSOR_CURRENT && recipe != FP8Q_RECIPE_TENSOR_DELAYED &&
+      recipe != FP8Q_RECIPE_BLOCK)
+    return FP8Q_ERR_INVALID_ARG;
+  if (recipe == FP8Q_RECIPE_TENSOR_DELAYED && (hist_x == nullptr || hist_w == nullptr))
+    return FP8Q_ERR_INVALID_ARG;
+  const size_t need = fp8q_linear_workspace_size(recipe, M, N, K);
+  if (workspace == nullptr || ws_bytes < need) return FP8Q_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FP8Q_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != FP8Q_OK) return rc;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  uint8_t *qx = ws;
+  ws += round256((size_t)(M * K));
+  uint8_t *qw = ws;
+  ws += round256((size_t)(N * K));
+  float *amax_x = reinterpret_cast<float *>(ws);
+  ws += round256(sizeof(float));
+  float *amax_w = reinterpret_cast<float *>(ws);
+  ws += round256(sizeof(float));
+  float *sx = reinterpret_cast<float *>(ws);
+  ws += round256(sizeof(float));
+  float *sw = reinterpret_cast<float *>(ws);
+  ws += round256(sizeof(float));
+
+  fp8q_operand A{}, B{};
+  A.data = qx;
+  A.format = FP8Q_E4M3;
+  B.data = qw;
+  B.format = FP8Q_E4M3;
+  if (recipe == FP8Q_RECIPE_BLOCK) {
+    float *x_scales = reinterpret_cast<float *>(ws);
+    ws += round256(sizeof(float) * (size_t)(((K + 127) / 128) * M));
+    float *w_scales = reinterpret_cast<float *>(ws);
+    if ((rc = fp8_quantize_tile1x128(x, in_dtype, M, K, FP8Q_E4M3, qx, x_scales, nullptr, nullptr,
+                                     0, stream)) != FP8Q_OK)
+      return rc;
+    if ((rc = fp8_quantize_block128x128(w, in_dtype, N, K, FP8Q_E4M3, qw, nullptr, w_scales, 0,
+                                        stream)) != FP8Q_OK)
+      return rc;
+    A.scaling = FP8Q_SCALE_TILE_1x128;
+    A.scale = x_scales;
+    A.scale_stride_row = 1;
+    A.scale_stride_k = M;
+    B.scaling = FP8Q_SCALE_BLOCK_128x128;
+    B.scale = w_scales;
+    B.scale_stride_row = (K + 127) / 128;
+    B.scale_stride_k = 1;
+  } else {
+    if (recipe == FP8Q_RECIPE_TENSOR_CURRENT) {
+      if ((rc = fp8_amax(x, in_dtype, M * K, amax_x, stream)) != FP8Q_OK) return rc;
+      if ((rc = fp8_amax(w, in_dtype, N * K, amax_w, stream)) != FP8Q_OK) return rc;
+      if ((rc = fp8_quantize_tensor(x, in_dtype, M, K, FP8Q_E4M3, amax_x, sx, qx, nullptr, 0,
+                                    stream)) != FP8Q_OK)
+        return rc;
+      if ((rc = fp8_quantize_tensor(w, in_dtype, N, K, FP8Q_E4M3, amax_w, sw, qw, nullptr, 0,
+                                    stream)) != FP8Q_OK)
+        return rc;
+    } else {
+      if ((rc = fp8_quantize_delayed(x, in_dtype, M, K, FP8Q_E4M3, hist_x, sx, qx, nullptr, 0,
+                                     stream)) != FP8Q_OK)
+        return rc;
+      if ((rc = fp8_quantize_delayed(w, in_dtype, N, K, FP8Q_E4M3, hist_w, sw, qw, nullptr, 0,
+                                     stream)) != FP8Q_OK)
+        return rc;
+    }
+    A.scaling = FP8Q_SCALE_TENSOR;
+    A.scale = sx;
+    B.scaling = FP8Q_SCALE_TENSOR;
+    B.scale = sw;
+  }
+  return fp8_gemm_fprop(&A, &B, y, out_dtype, M, N, K, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,636 @@
+// Steps a4-a5 of the path: the FP8 GEMM C = A . B^T with dequantising scales
+// ("fp8_parity.py", FP8Matmul: xq @ wq.T; the blog repost's Fprop / Dgrad /
+// Wgrad shapes), on the 5th-generation tensor cores.
+//
+// Both kernels are persistent (one CTA per SM, static round-robin over output
+// tiles grouped 16 M-tiles at a time for L2 reuse) and warp-specialised:
+//   warp 0   TMA producer: 128x128-byte A and BNx128-byte B boxes, 128-byte
+//            swizzle, into a STAGES-deep shared-memory ring (full/empty
+//            mbarriers);
+//   warp 1   allocates TMEM and issues tcgen05.mma.kind::f8f6f4 (M = 128,
+//            N = BN, K = 32 per instruction, four per 128-byte K block) from
+//            one thread; tcgen05.commit releases ring slots and hands
+//            accumulators on;
+//   warps 2+ epilogue (per-tensor kernel) or promotion + epilogue (block
+//            kernel): tcgen05.ld from TMEM, scale, convert, store.
+// Per-tensor scaling accumulates the whole K range in TMEM (two accumulator
+// buffers so one tile's epilogue overlaps the next tile's MMAs) and applies
+// s_A s_B once.  Tile/block scaling accumulates each 128-wide K block into a
+// ping-pong TMEM buffer; the promotion warps add it into fp32 registers with
+// that block's s_A(m, kb) s_B(n, kb) (the blocked sum of the definition).
+//
+// Every mbarrier wait is bounded (about two seconds of wall time); on expiry
+// the kernel records FP8Q_ERR_TIMEOUT in the device error word, drains what
+// it issued, frees its TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "fp8q_internal.h"
+#include "fp8q_ptx.cuh"
+
+namespace fp8q {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;
+constexpr int kBK = 128;            // bytes = FP8 elements per K block
+constexpr int kUmmaK = 32;          // K per tcgen05.mma for 8-bit inputs
+constexpr int kGroupM = 16;         // M-tiles per raster group
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+struct GemmArgs {
+  int64_t M, N, K;
+  int num_m_tiles, num_n_tiles, num_k_blocks;
+  uint32_t idesc;
+  void *C;
+  // per-tensor scales (device scalars)
+  const float *scale_a;
+  const float *scale_b;
+  // tile / block scales
+  int64_t a_stride_row, a_stride_k;
+  int64_t b_stride_row, b_stride_k;
+  unsigned int *err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mt, int &nt) {
+  const int per_group = kGroupM * num_n;
+  const int g = tile / per_group;
+  const int first_m = g * kGroupM;
+  const int gsize = min(num_m - first_m, kGroupM);
+  const int local = tile - g * per_group;
+  mt = first_m + local % gsize;
+  nt = local / gsize;
+}
+
+// Bounded wait.  Returns false when the CTA is aborting (this call timed out
+// or another role already did).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int *abort_flag, unsigned int *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform variant: lane 0 waits, the verdict is broadcast.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag, unsigned int *err) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, err) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  return ok != 0;
+}
+
+template <int BN, int STAGES>
+struct Layout {
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 5);  // full, empty, acc full/empty x2, drain
+  static constexpr int kSmemBytes = kRingBytes + kBarBytes + 16 + 1024;  // + align slack
+};
+
+// Producer loop shared by both kernels.
+template <int BN, int STAGES>
+__device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUtensorMap *tb,
+                                              const GemmArgs &p, uint32_t ring, uint32_t bars,
+                                              volatile int *abort_flag) {
+  using L = Layout<BN, STAGES>;
+  const int total = p.num_m_tiles * p.num_n_tiles;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    int mt, nt;
+    tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
+    for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+      const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+      const uint32_t full = bars + 8 * s, empty = bars + 8 * (STAGES + s);
+      if (!wait_bounded(empty, ph ^ 1u, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sa = ring + s * L::kStageBytes;
+      mbar_arrive_expect_tx(full, L::kStageBytes);
+      tma_load_2d(sa, ta, kb * kBK, mt * kBM, full);
+      tma_load_2d(sa + L::kABytes, tb, kb * kBK, nt * BN, full);
+    }
+  }
+  if (!ok) {
+    // Let the copies already issued land before the CTA goes away.
+    const uint32_t n = it < (uint32_t)STAGES ? it : (uint32_t)STAGES;
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t jj = it - 1 - j;
+      const uint32_t s = jj % STAGES, ph = (jj / STAGES) & 1u;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bars + 8 * s, ph) && globaltimer_ns() - t0 < 200000000ull) {
+      }
+    }
+  }
+}
+
+// MMAs of one 128-byte K block held in ring slot `s`.
+template <int BN, int STAGES>
+__device__ __forceinline__ void issue_kblock(uint32_t ring, uint32_t s, uint32_t d_tmem,
+                                             uint32_t idesc, bool accumulate_first) {
+  using L = Layout<BN, STAGES>;
+  const uint32_t a0 = ring + s * L::kStageBytes;
+  const uint32_t b0 = a0 + L::kABytes;
+#pragma unroll
+  for (int k = 0; k < kBK / kUmmaK; ++k) {
+    const uint64_t ad = sdesc_k_sw128(a0 + k * kUmmaK);
+    const uint64_t bd = sdesc_k_sw128(b0 + k * kUmmaK);
+    mma_f8f6f4(d_tmem, ad, bd, idesc, (accumulate_first || k > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void drain_mma(uint32_t drain_bar, volatile int *abort_flag) {
+  // Completion of everything this thread issued: commit to a private barrier
+  // and wait for its first phase (bounded).
+  mma_commit(drain_bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < 200000000ull) {
+  }
+  (void)abort_flag;
+}
+
+// Store 32 consecutive fp32 results (already scaled) of row m starting at
+// column n0; columns >= N are skipped in groups of 8 (N % 16 == 0).
+template <bool OUT_BF16>
+__device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n0,
+                                        const float (&v)[32]) {
+  if (OUT_BF16) {
+    __nv_bfloat16 *row = static_cast<__nv_bfloat16 *>(C) + m * N;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      if (n0 + 8 * g < N) {
+        uint32_t w[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          __nv_bfloat162 b = __floats2bfloat162_rn(v[8 * g + 2 * h], v[8 * g + 2 * h + 1]);
+          w[h] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        *reinterpret_cast<uint4 *>(row + n0 + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  } else {
+    float *row = static_cast<float *>(C) + m * N;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      if (n0 + 4 * g < N)
+        *reinterpret_cast<float4 *>(row + n0 + 4 * g) =
+            make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------
+// Per-tensor scaled GEMM: 6 warps (producer, MMA, 4 epilogue warps).
+// ------------------------------------------------------------------------
+template <int BN, int STAGES, bool OUT_BF16>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tensor_kernel(const __grid_constant__ CUtensorMap ta,
+                       const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
+  using L = Layout<BN, STAGES>;
+  constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // 128, 256 or 512
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t bars = ring + L::kRingBytes;
+  const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
+  const uint32_t accf0 = bars + 8 * (2 * STAGES), acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  const uint32_t slot = bars + L::kBarBytes;  // TMEM base address written here
+  uint8_t *slot_ptr = smem_raw + (slot - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    prefetch_tmap(&ta);
+    prefetch_tmap(&tb);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
+  const int total = p.num_m_tiles * p.num_n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++acc_it) {
+        const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+        if (!wait_bounded(acce0 + 8 * buf, aph ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_kblock<BN, STAGES>(ring, s, d_tmem, p.idesc, kb > 0);
+          mma_commit(empty0 + 8 * s);
+        }
+        if (!ok) break;
+        mma_commit(accf0 + 8 * buf);
+      }
+      drain_mma(drain, abort_flag);
+    }
+    __syncwarp();
+  } else {
+    // Epilogue warps 2..5 -> TMEM lane quarters 2, 3, 0, 1.
+    const int quarter = warp & 3;
+    const float scale = __fmul_rn(p.scale_a[0], p.scale_b[0]);
+    uint32_t acc_it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++acc_it) {
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
+      const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+      if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + c * 32, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
+        const int64_t n0 = (int64_t)nt * BN + c * 32;
+        if (m < p.M && n0 < p.N) store32<OUT_BF16>(p.C, p.N, m, n0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------------
+// Tile/block scaled GEMM: 12 warps -- warpgroup 0 holds the producer (warp 0)
+// and the MMA issuer (warp 1); warpgroups 1 and 2 are promotion warps, each
+// warpgroup owning 128 of the 256 tile columns.  A carries 1x128
+// tile scales; B carries 128x128 block scales (B_TILE = false) or 1x128 tile
+// scales (B_TILE = true).
+// ------------------------------------------------------------------------
+constexpr int kBSBN = 256;
+constexpr int kBSStages = 4;
+constexpr int kBSThreads = 384;  // 168 registers per thread at one CTA per SM
+
+template <bool B_TILE, bool OUT_BF16>
+__global__ void __launch_bounds__(kBSThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap ta,
+                            const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
+  constexpr int BN = kBSBN, STAGES = kBSStages;
+  using L = Layout<BN, STAGES>;
+  constexpr uint32_t kTmemCols = 512;  // two 256-column partial-sum buffers
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(16) float sh_bscale[8][128];  // per promotion warp: B tile scales
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t bars = ring + L::kRingBytes;
+  const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
+  const uint32_t pf0 = bars + 8 * (2 * STAGES), pe0 = pf0 + 16;
+  const uint32_t drain = pe0 + 16;
+  const uint32_t slot = bars + L::kBarBytes;
+  uint8_t *slot_ptr = smem_raw + (slot - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(pf0 + 8 * b, 1);
+      mbar_init(pe0 + 8 * b, 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    prefetch_tmap(&ta);
+    prefetch_tmap(&tb);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
+  const int total = p.num_m_tiles * p.num_n_tiles;
+  const int nkb = p.num_k_blocks;
+
+  if (warp == 0) {
+    if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+          if (!wait_bounded(pe0 + 8 * pb, pph ^ 1u, abort_flag, p.err) ||
+              !wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
+          mma_commit(empty0 + 8 * s);
+          mma_commit(pf0 + 8 * pb);
+        }
+      }
+      drain_mma(drain, abort_flag);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // Promotion warps 4..11: warpgroup wg owns tile columns [128 wg, 128 wg + 128);
+    // TMEM lane quarter = warp % 4.  Scales for K block kb + 1 are fetched
+    // into registers while block kb is promoted; B tile scales go through a
+    // per-warp shared buffer guarded by __syncwarp only (no cross-warp
+    // barrier, so an aborting warp can never strand the others).
+    const int pw = warp - 4;           // 0..7
+    const int wg = pw >> 2;
+    const int quarter = warp & 3;
+    float *my_bs = sh_bscale[pw];
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
+      const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
+      const bool m_ok = m < p.M;
+      const int64_t ncol0 = (int64_t)nt * BN + wg * 128;  // first column of this warpgroup
+      const int64_t nblk = ncol0 / 128;
+      const bool nblk_ok = ncol0 < p.N;
+      const int64_t nl = ncol0 + lane * 4;                 // this lane's 4 B-scale columns
+      auto load_sa = [&](int kb) -> float {
+        return m_ok ? p.scale_a[kb * p.a_stride_k + m * p.a_stride_row] : 0.0f;
+      };
+      auto load_sb = [&](int kb) -> float {
+        return nblk_ok ? p.scale_b[nblk * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
+      };
+      auto load_sb4 = [&](int kb) -> float4 {
+        float4 f;
+        const float *base = p.scale_b + kb * p.b_stride_k;
+        f.x = (nl + 0 < p.N) ? base[(nl + 0) * p.b_stride_row] : 0.0f;
+        f.y = (nl + 1 < p.N) ? base[(nl + 1) * p.b_stride_row] : 0.0f;
+        f.z = (nl + 2 < p.N) ? base[(nl + 2) * p.b_stride_row] : 0.0f;
+        f.w = (nl + 3 < p.N) ? base[(nl + 3) * p.b_stride_row] : 0.0f;
+        return f;
+      };
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      float sa_next = load_sa(0);
+      float sb_next = B_TILE ? 0.0f : load_sb(0);
+      float4 sb4_next = B_TILE ? load_sb4(0) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const float sa = sa_next;
+        const float sb = sb_next;
+        const float4 sb4 = sb4_next;
+        if (kb + 1 < nkb) {
+          sa_next = load_sa(kb + 1);
+          if (B_TILE) sb4_next = load_sb4(kb + 1);
+          else sb_next = load_sb(kb + 1);
+        }
+        if (B_TILE) {
+          __syncwarp();
+          *reinterpret_cast<float4 *>(&my_bs[lane * 4]) = sb4;
+          __syncwarp();
+        }
+        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        if (!wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sab = __fmul_rn(sa, sb);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(
+              tmem_base + ((uint32_t)(quarter * 32) << 16) + pb * BN + wg * 128 + c * 16, r);
+          tmem_ld_wait();
+          if (c == 7) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pe0 + 8 * pb);
+          }
+          if (B_TILE) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[c * 16 + j] = __fmaf_rn(__uint_as_float(r[j]), __fmul_rn(sa, my_bs[c * 16 + j]),
+                                          acc[c * 16 + j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[c * 16 + j] = __fmaf_rn(__uint_as_float(r[j]), sab, acc[c * 16 + j]);
+          }
+        }
+      }
+      if (!ok) break;
+      if (m_ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int64_t n0 = ncol0 + c * 32;
+          if (n0 < p.N) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
+            store32<OUT_BF16>(p.C, p.N, m, n0, v);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, K] byte matrix, box = box_k x box_rows, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K, uint32_t box_k,
+               uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[2] = {K, rows};
+  cuuint64_t gstride[1] = {K};
+  cuuint32_t box[2] = {box_k, box_rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), gdim, gstride,
+                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename KernelT>
+cudaError_t set_smem(KernelT kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int BN, int STAGES, bool OUT_BF16>
+int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
+               cudaStream_t stream) {
+  using L = Layout<BN, STAGES>;
+  auto kernel = gemm_tensor_kernel<BN, STAGES, OUT_BF16>;
+  static bool attr_done = false;  // per instantiation
+  if (!attr_done) {
+    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    attr_done = true;
+  }
+  kernel<<<grid, 192, L::kSmemBytes, stream>>>(ta, tb, a);
+  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+template <bool B_TILE, bool OUT_BF16>
+int run_blockscaled(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
+                    cudaStream_t stream) {
+  using L = Layout<kBSBN, kBSStages>;
+  auto kernel = gemm_blockscaled_kernel<B_TILE, OUT_BF16>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    attr_done = true;
+  }
+  kernel<<<grid, kBSThreads, L::kSmemBytes, stream>>>(ta, tb, a);
+  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int out_dtype,
+                int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+  const bool bf16 = out_dtype == FP8Q_DT_BF16;
+  if (M == 0 || N == 0) return FP8Q_OK;
+  if (K == 0) {
+    return cudaMemsetAsync(C, 0, (size_t)(M * N) * (bf16 ? 2 : 4), stream) == cudaSuccess
+               ? FP8Q_OK
+               : FP8Q_ERR_CUDA;
+  }
+  const bool tensor = A.scaling == FP8Q_SCALE_TENSOR && B.scaling == FP8Q_SCALE_TENSOR;
+  if (!tensor) {
+    if (A.scaling != FP8Q_SCALE_TILE_1x128 ||
+        (B.scaling != FP8Q_SCALE_TILE_1x128 && B.scaling != FP8Q_SCALE_BLOCK_128x128))
+      return FP8Q_ERR_NOT_IMPLEMENTED;
+  }
+  int BN = 256;
+  if (tensor) BN = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, kBK, kBM) ||
+      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, kBK, (uint32_t)BN))
+    return FP8Q_ERR_CUDA;
+
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_m_tiles = (int)((M + kBM - 1) / kBM);
+  a.num_n_tiles = (int)((N + BN - 1) / BN);
+  a.num_k_blocks = (int)((K + kBK - 1) / kBK);
+  a.idesc = ptx::idesc_f8f6f4((uint32_t)A.format, (uint32_t)B.format, kBM, (uint32_t)BN);
+  a.C = C;
+  a.scale_a = A.scale;
+  a.scale_b = B.scale;
+  a.a_stride_row = A.stride_row;
+  a.a_stride_k = A.stride_k;
+  a.b_stride_row = B.stride_row;
+  a.b_stride_k = B.stride_k;
+  a.err = device_error_word();
+  if (a.err == nullptr) return FP8Q_ERR_CUDA;
+  const int64_t tiles = (int64_t)a.num_m_tiles * a.num_n_tiles;
+  if (tiles > INT32_MAX / 2) return FP8Q_ERR_INVALID_ARG;
+  int grid = sm_count();
+  if (tiles < grid) grid = (int)tiles;
+
+  if (tensor) {
+    if (BN == 64)
+      return bf16 ? run_tensor<64, 8, true>(ta, tb, a, grid, stream)
+                  : run_tensor<64, 8, false>(ta, tb, a, grid, stream);
+    if (BN == 128)
+      return bf16 ? run_tensor<128, 6, true>(ta, tb, a, grid, stream)
+                  : run_tensor<128, 6, false>(ta, tb, a, grid, stream);
+    return bf16 ? run_tensor<256, 4, true>(ta, tb, a, grid, stream)
+                : run_tensor<256, 4, false>(ta, tb, a, grid, stream);
+  }
+  const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
+  if (b_tile)
+    return bf16 ? run_blockscaled<true, true>(ta, tb, a, grid, stream)
+                : run_blockscaled<true, false>(ta, tb, a, grid, stream);
+  return bf16 ? run_blockscaled<false, true>(ta, tb, a, grid, stream)
+              : run_blockscaled<false, false>(ta, tb, a, grid, stream);
+}
+
+}  // namespace fp8q

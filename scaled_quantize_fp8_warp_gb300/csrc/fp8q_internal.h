@@ -1,0 +1,61 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8q.h"
+
+namespace fp8q {
+
+constexpr int kNumSMsHint = 152;
+
+// Device error word of the current device (set by kernels whose bounded
+// waits expire).  Defined in fp8q_api.cu.
+unsigned int *device_error_word();
+
+// SM count of the current device (cached).
+int sm_count();
+
+enum QuantMode : int {
+  kModeTensorCurrent = 0,  // s from a device amax
+  kModeTensorDelayed = 1,  // s from a device amax history, amax(x) pushed
+  kModeTile = 2,           // 1x128 row tiles and/or 128x1 column tiles
+  kModeBlock = 3           // 128x128 blocks
+};
+
+struct QuantParams {
+  const void *x;
+  int64_t rows, cols;
+  int in_dtype;   // FP8Q_DT_*
+  int format;     // FP8Q_E4M3 / FP8Q_E5M2
+  int saturate;
+  int mode;       // QuantMode
+  const float *amax_in;        // kModeTensorCurrent
+  fp8q_amax_history *hist;     // kModeTensorDelayed
+  float *scale_out;            // tensor modes, nullable
+  uint8_t *q;                  // [rows, cols] or null
+  uint8_t *q_t;                // [cols, rows] or null
+  float *q_scales;             // tile: [ceil(cols/128), rows]; block: [nrb, ncb]
+  float *qt_scales;            // tile: [ceil(rows/128), cols]
+};
+
+cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
+                        cudaStream_t stream);
+cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream);
+
+struct GemmOperandDev {
+  const uint8_t *data;
+  int format;
+  int scaling;
+  const float *scale;
+  int64_t stride_row;
+  int64_t stride_k;
+};
+
+// C[M,N] = A[M,K] . B[N,K]^T with dequantising scales.
+int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C,
+                int out_dtype, int64_t M, int64_t N, int64_t K,
+                cudaStream_t stream);
+
+}  // namespace fp8q

@@ -1,0 +1,576 @@
+// Steps a1-a3 of the path: amax reduction, fp32 scale, RNE cast to FP8.
+//
+// Definitions ("fp8_parity.py", scaled_roundtrip): s = (amax / fmax) clamped
+// below at 1e-12, byte = (x / s).to(fp8).  The quotient must be the correctly
+// rounded fp32 division.  Per scale we form r = RN(1/s) once and, per element,
+//   q0 = RN(x r);  e = x - q0 s (exact, one FMA);  q = RN(q0 + e r)
+// which is Markstein's correction step (P. Markstein, IBM J. Res. Dev. 34(1),
+// 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. on
+// division): with r within half an ulp of 1/s it returns RN(x / s) whenever
+// the remainder does not underflow.  Here s >= 1e-12, so a remainder can only
+// underflow for |x / s| < 2^-63, where every FP8 code is a signed zero; the
+// sign is restored with copysign.  The correction is only used on data whose
+// quotients stay below the FP8 overflow point (checked per thread, row,
+// column or block from the amax already at hand); anything else -- Inf or NaN
+// scales or data, overflowing quotients -- takes true IEEE division and the
+// explicit NaN / Inf / saturation rules.
+//
+// Kernel layout: one CTA of 256 threads owns a 128x128 input tile at a time
+// (grid-stride over tiles).  Thread (warp w, lane l) holds rows
+// [8 rg, 8 rg + 8) and columns [8 cg, 8 cg + 8) of the tile with
+// rg = 2 w + l / 16, cg = l % 16: eight 16-byte loads, each warp instruction
+// covering two full 256-byte row segments (bf16).  Row amax for 1x128 tiles
+// is a shuffle butterfly inside each half-warp; column amax for 128x1 tiles
+// goes through shared memory; the transposed FP8 copy is an in-register 8x8
+// byte transpose (uniform scales) or a second cast (column-tile scales).
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "fp8q_internal.h"
+
+namespace fp8q {
+namespace {
+
+constexpr int kQuantThreads = 256;
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<FP8Q_E4M3> {
+  static constexpr float kMax = 448.0f;
+  static constexpr float kFastLimit = 460.0f;  // below the 464 overflow midpoint
+  static constexpr __nv_fp8_interpretation_t kInterp = __NV_E4M3;
+};
+template <>
+struct FmtTraits<FP8Q_E5M2> {
+  static constexpr float kMax = 57344.0f;
+  static constexpr float kFastLimit = 61000.0f;  // below the 61440 midpoint
+  static constexpr __nv_fp8_interpretation_t kInterp = __NV_E5M2;
+};
+
+__device__ __forceinline__ uint32_t abs_bits(float v) {
+  return __float_as_uint(v) & 0x7FFFFFFFu;
+}
+
+// s = max(fl32(amax / fmax), fl32(1e-12)); a NaN amax gives a NaN scale.
+__device__ __forceinline__ float scale_from_amax(float amax, float fm) {
+  float s = __fdiv_rn(amax, fm);
+  return (s < 1e-12f) ? 1e-12f : s;
+}
+
+// Correctly rounded x / s given r = RN(1/s) (see the file comment).
+__device__ __forceinline__ float div_fast(float x, float s, float r) {
+  float q0 = __fmul_rn(x, r);
+  float e = __fmaf_rn(-q0, s, x);
+  float q1 = __fmaf_rn(e, r, q0);
+  return copysignf(q1, q0);
+}
+
+// Two fp32 values -> two FP8 bytes (lo in the low byte), RNE, saturating.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE,
+                                             FmtTraits<FMT>::kInterp);
+}
+
+// Full-rule encode for the slow path: NaN -> 0x7F | sign; without saturation
+// an overflowing quotient becomes NaN (E4M3) or Inf (E5M2).
+template <int FMT>
+__device__ __forceinline__ uint32_t encode_slow(float v, int saturate) {
+  uint32_t sgn = (__float_as_uint(v) >> 24) & 0x80u;
+  if (v != v) return 0x7Fu | sgn;
+  if (!saturate) {
+    float a = fabsf(v);
+    if (FMT == FP8Q_E4M3) {
+      if (a > 464.0f) return 0x7Fu | sgn;
+    } else {
+      if (a >= 61440.0f) return 0x7Cu | sgn;
+    }
+  }
+  return cvt2<FMT>(v, 0.0f) & 0xFFu;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 cast8_fast(const float (&v)[8], float s, float r) {
+  uint32_t p0 = cvt2<FMT>(div_fast(v[0], s, r), div_fast(v[1], s, r));
+  uint32_t p1 = cvt2<FMT>(div_fast(v[2], s, r), div_fast(v[3], s, r));
+  uint32_t p2 = cvt2<FMT>(div_fast(v[4], s, r), div_fast(v[5], s, r));
+  uint32_t p3 = cvt2<FMT>(div_fast(v[6], s, r), div_fast(v[7], s, r));
+  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+}
+
+template <int FMT>
+__device__ __noinline__ uint2 cast8_slow(const float (&v)[8], float s, int saturate) {
+  uint32_t b[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) b[j] = encode_slow<FMT>(__fdiv_rn(v[j], s), saturate);
+  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
+                    b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(const float (&v)[8], float s, float r, bool fast,
+                                       int saturate) {
+  if (fast) return cast8_fast<FMT>(v, s, r);
+  return cast8_slow<FMT>(v, s, saturate);
+}
+
+// Quotients of every value with |x| <= m stay on the fast path's domain.
+template <int FMT>
+__device__ __forceinline__ bool fast_ok(uint32_t m_bits, float r) {
+  return (r > 0.0f) && (__uint_as_float(m_bits) * r <= FmtTraits<FMT>::kFastLimit);
+}
+
+// Eight consecutive input elements of one row, kept in their storage type
+// (bf16 stays packed two to a register).  at(j) widens element j to fp32.
+template <typename InT>
+struct Row8;
+
+template <>
+struct Row8<uint16_t> {
+  uint4 w;
+  __device__ __forceinline__ void load(const void *base, int64_t idx) {
+    w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
+  }
+  __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ uint32_t word(int k) const {
+    return k == 0 ? w.x : (k == 1 ? w.y : (k == 2 ? w.z : w.w));
+  }
+  __device__ __forceinline__ float at(int j) const {
+    const uint32_t x = word(j >> 1);
+    return (j & 1) ? __uint_as_float(x & 0xFFFF0000u) : __uint_as_float(x << 16);
+  }
+  // max |element| as an fp32 bit pattern
+  __device__ __forceinline__ uint32_t absmax_bits() const {
+    const uint32_t k = 0x7FFF7FFFu;
+    const uint32_t m = __vmaxu2(__vmaxu2(w.x & k, w.y & k), __vmaxu2(w.z & k, w.w & k));
+    return max(m & 0xFFFFu, m >> 16) << 16;
+  }
+  // per-column running max |x|, packed: cm[k] holds columns 2k, 2k+1
+  static constexpr int kColWords = 4;
+  __device__ __forceinline__ void colmax_update(uint32_t (&cm)[kColWords]) const {
+    const uint32_t k = 0x7FFF7FFFu;
+    cm[0] = __vmaxu2(cm[0], w.x & k);
+    cm[1] = __vmaxu2(cm[1], w.y & k);
+    cm[2] = __vmaxu2(cm[2], w.z & k);
+    cm[3] = __vmaxu2(cm[3], w.w & k);
+  }
+  __device__ __forceinline__ static uint32_t colmax_bits(const uint32_t (&cm)[kColWords], int j) {
+    const uint32_t x = cm[j >> 1];
+    return (j & 1) ? (x & 0xFFFF0000u) : (x << 16);
+  }
+};
+
+template <>
+struct Row8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const void *base, int64_t idx) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + idx);
+    a = __ldg(p);
+    b = __ldg(p + 1);
+  }
+  __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ float at(int j) const {
+    switch (j) {
+      case 0: return a.x; case 1: return a.y; case 2: return a.z; case 3: return a.w;
+      case 4: return b.x; case 5: return b.y; case 6: return b.z; default: return b.w;
+    }
+  }
+  __device__ __forceinline__ uint32_t absmax_bits() const {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = max(m, abs_bits(at(j)));
+    return m;
+  }
+  static constexpr int kColWords = 8;
+  __device__ __forceinline__ void colmax_update(uint32_t (&cm)[kColWords]) const {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cm[j] = max(cm[j], abs_bits(at(j)));
+  }
+  __device__ __forceinline__ static uint32_t colmax_bits(const uint32_t (&cm)[kColWords], int j) {
+    return cm[j];
+  }
+};
+
+template <int FMT, typename InT>
+__device__ __forceinline__ uint2 cast_row(const Row8<InT> &x, float s, float r, bool fast,
+                                          int saturate) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = x.at(j);
+  return cast8<FMT>(v, s, r, fast, saturate);
+}
+
+// 4x4 byte transpose: a..d are rows (byte k = column k); o0..o3 are columns.
+__device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                             uint32_t &o0, uint32_t &o1, uint32_t &o2,
+                                             uint32_t &o3) {
+  uint32_t t0 = __byte_perm(a, b, 0x5140);
+  uint32_t t1 = __byte_perm(a, b, 0x7362);
+  uint32_t t2 = __byte_perm(c, d, 0x5140);
+  uint32_t t3 = __byte_perm(c, d, 0x7362);
+  o0 = __byte_perm(t0, t2, 0x5410);
+  o1 = __byte_perm(t0, t2, 0x7632);
+  o2 = __byte_perm(t1, t3, 0x5410);
+  o3 = __byte_perm(t1, t3, 0x7632);
+}
+
+// rows[i] holds row i (8 bytes, columns 0..7); cols[j] receives column j.
+__device__ __forceinline__ void transpose8x8(const uint2 (&rows)[8], uint2 (&cols)[8]) {
+  transpose4x4(rows[0].x, rows[1].x, rows[2].x, rows[3].x, cols[0].x, cols[1].x, cols[2].x,
+               cols[3].x);
+  transpose4x4(rows[4].x, rows[5].x, rows[6].x, rows[7].x, cols[0].y, cols[1].y, cols[2].y,
+               cols[3].y);
+  transpose4x4(rows[0].y, rows[1].y, rows[2].y, rows[3].y, cols[4].x, cols[5].x, cols[6].x,
+               cols[7].x);
+  transpose4x4(rows[4].y, rows[5].y, rows[6].y, rows[7].y, cols[4].y, cols[5].y, cols[6].y,
+               cols[7].y);
+}
+
+// Kernel variants.
+enum KernelMode : int {
+  kKTensor = 0,     // uniform scale from a device amax
+  kKDelayed = 1,    // uniform scale from the history, amax pushed after
+  kKTileRow = 2,    // 1x128 row tiles -> q, q_scales
+  kKTileCol = 3,    // 128x1 column tiles -> q_t, qt_scales
+  kKTileBoth = 4,   // both from one read
+  kKBlock = 5       // 128x128 blocks -> q and/or q_t, block scales
+};
+
+template <typename InT, int FMT, int KM>
+__global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantParams p) {
+  constexpr bool kRowTiles = (KM == kKTileRow || KM == kKTileBoth);
+  constexpr bool kColTiles = (KM == kKTileCol || KM == kKTileBoth);
+  constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock);
+  const float fm = FmtTraits<FMT>::kMax;
+
+  __shared__ float sh_row_s[128], sh_row_r[128];
+  __shared__ float sh_col_s[128], sh_col_r[128];
+  __shared__ uint32_t sh_colmax[8][128];
+  __shared__ uint32_t sh_red[8];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rg = warp * 2 + (lane >> 4);
+  const int cg = lane & 15;
+  const int64_t rows = p.rows, cols = p.cols;
+  const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
+  const int64_t ntiles = tiles_r * tiles_c;
+  const int saturate = p.saturate;
+
+  float s_u = 0.0f, r_u = 0.0f;
+  if (KM == kKTensor) {
+    s_u = scale_from_amax(*p.amax_in, fm);
+    r_u = __fdiv_rn(1.0f, s_u);
+  } else if (KM == kKDelayed) {
+    uint32_t h = 0;
+#pragma unroll
+    for (int i = 0; i < FP8Q_HISTORY_LEN; ++i) h = max(h, abs_bits(p.hist->amax[i]));
+    s_u = scale_from_amax(__uint_as_float(h), fm);
+    r_u = __fdiv_rn(1.0f, s_u);
+  }
+  uint32_t run_max = 0;  // delayed: running max |x| of this CTA
+
+  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    // Per-tensor current scaling runs right after the amax pass over the same
+    // data; walking the tiles backwards meets the most recently read (still
+    // L2-resident) part of x first.
+    const int64_t tt = (KM == kKTensor) ? (ntiles - 1 - t) : t;
+    const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
+    const int64_t r0 = tr * 128, c0 = tc * 128;
+    const int64_t cbase = c0 + cg * 8;
+    const int64_t rbase = r0 + rg * 8;
+    const bool col_ok = cbase < cols;
+    const bool rchunk_ok = rbase < rows;
+
+    Row8<InT> v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (col_ok && rbase + i < rows) v[i].load(p.x, (rbase + i) * cols + cbase);
+      else v[i].zero();
+    }
+
+    uint32_t rowmax[8];
+    uint32_t cmp[Row8<InT>::kColWords];
+    uint32_t tmax = 0;
+    if (kRowTiles || kUniform) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rowmax[i] = v[i].absmax_bits();
+    }
+    if (kColTiles) {
+#pragma unroll
+      for (int k = 0; k < Row8<InT>::kColWords; ++k) cmp[k] = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i].colmax_update(cmp);
+    }
+    if (kUniform) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) tmax = max(tmax, rowmax[i]);
+    }
+
+    // ------------------------------------------------ uniform-scale modes
+    if (kUniform) {
+      float s = s_u, r = r_u;
+      if (KM == kKBlock) {
+        uint32_t m = __reduce_max_sync(0xFFFFFFFFu, tmax);
+        if (lane == 0) sh_red[warp] = m;
+        __syncthreads();
+        uint32_t bm = sh_red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) bm = max(bm, sh_red[w]);
+        s = scale_from_amax(__uint_as_float(bm), fm);
+        r = __fdiv_rn(1.0f, s);
+        if (tid == 0) p.q_scales[tr * tiles_c + tc] = s;
+      }
+      if (KM == kKDelayed) run_max = max(run_max, tmax);
+      const bool fast = fast_ok<FMT>(tmax, r);
+      uint2 rb[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rb[i] = cast_row<FMT>(v[i], s, r, fast, saturate);
+      if (p.q != nullptr && col_ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (rbase + i < rows)
+            *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = rb[i];
+      }
+      if (p.q_t != nullptr && col_ok && rchunk_ok) {
+        uint2 cb[8];
+        transpose8x8(rb, cb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = cb[j];
+      }
+    }
+
+    // ------------------------------------------------------ 1x128 row tiles
+    if (kRowTiles) {
+      // Butterfly over the 16 lanes of a half-warp that share these 8 rows:
+      // each exchange halves the rows a lane keeps, so 8 shuffles reduce all
+      // 8 rows.  Afterwards lanes cg and cg^1 hold the max of row
+      // rsel = 4 b3 + 2 b2 + b1 (b_k = bit k of cg).
+      const bool h3 = cg & 8, h2 = cg & 4, h1 = cg & 2;
+      uint32_t a4[4];
+#pragma unroll
+      for (int t4 = 0; t4 < 4; ++t4) {
+        uint32_t keep = h3 ? rowmax[t4 + 4] : rowmax[t4];
+        uint32_t send = h3 ? rowmax[t4] : rowmax[t4 + 4];
+        a4[t4] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+      }
+      uint32_t a2[2];
+#pragma unroll
+      for (int t2 = 0; t2 < 2; ++t2) {
+        uint32_t keep = h2 ? a4[t2 + 2] : a4[t2];
+        uint32_t send = h2 ? a4[t2] : a4[t2 + 2];
+        a2[t2] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+      }
+      uint32_t a1 = max(h1 ? a2[1] : a2[0], __shfl_xor_sync(0xFFFFFFFFu, h1 ? a2[0] : a2[1], 2));
+      a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, 1));
+      const int rsel = (h3 ? 4 : 0) + (h2 ? 2 : 0) + (h1 ? 1 : 0);
+      if ((cg & 1) == 0) {
+        float s = scale_from_amax(__uint_as_float(a1), fm);
+        sh_row_s[rg * 8 + rsel] = s;
+        sh_row_r[rg * 8 + rsel] = __fdiv_rn(1.0f, s);
+        if (rbase + rsel < rows) p.q_scales[tc * rows + rbase + rsel] = s;
+      }
+      __syncwarp();
+      if (col_ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float s = sh_row_s[rg * 8 + i], r = sh_row_r[rg * 8 + i];
+          uint2 b = cast_row<FMT>(v[i], s, r, fast_ok<FMT>(rowmax[i], r), saturate);
+          if (rbase + i < rows) *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = b;
+        }
+      }
+    }
+
+    // --------------------------------------------------- 128x1 column tiles
+    if (kColTiles) {
+      uint32_t colmax[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        colmax[j] = Row8<InT>::colmax_bits(cmp, j);
+        colmax[j] = max(colmax[j], __shfl_xor_sync(0xFFFFFFFFu, colmax[j], 16));
+      }
+      if (lane < 16) {
+        *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8]) =
+            make_uint4(colmax[0], colmax[1], colmax[2], colmax[3]);
+        *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8 + 4]) =
+            make_uint4(colmax[4], colmax[5], colmax[6], colmax[7]);
+      }
+      __syncthreads();
+      if (tid < 128) {
+        uint32_t m = sh_colmax[0][tid];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = max(m, sh_colmax[w][tid]);
+        float s = scale_from_amax(__uint_as_float(m), fm);
+        sh_col_s[tid] = s;
+        sh_col_r[tid] = __fdiv_rn(1.0f, s);
+        if (c0 + tid < cols) p.qt_scales[tr * cols + c0 + tid] = s;
+      }
+      __syncthreads();
+      if (col_ok && rchunk_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float s = sh_col_s[cg * 8 + j], r = sh_col_r[cg * 8 + j];
+          float cv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
+          uint2 b = cast8<FMT>(cv, s, r, fast_ok<FMT>(colmax[j], r), saturate);
+          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = b;
+        }
+      }
+    }
+    __syncthreads();  // shared scratch is reused by the next tile
+  }
+
+  // ------------------------------------------ per-tensor scale bookkeeping
+  if (KM == kKTensor) {
+    if (blockIdx.x == 0 && tid == 0 && p.scale_out != nullptr) *p.scale_out = s_u;
+  }
+  if (KM == kKDelayed) {
+    uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run_max);
+    if (lane == 0) sh_red[warp] = m;
+    __syncthreads();
+    if (tid == 0) {
+      uint32_t cm = sh_red[0];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) cm = max(cm, sh_red[w]);
+      fp8q_amax_history *h = p.hist;
+      atomicMax(&h->pending, cm);
+      __threadfence();
+      const unsigned prev = atomicAdd(&h->arrivals, 1u);
+      if (prev == gridDim.x - 1) {
+        // Last CTA: every other CTA has read the history and published its
+        // amax.  Push the tensor's amax into the ring and reset the scratch.
+        __threadfence();
+        const uint32_t amax_bits = atomicExch(&h->pending, 0u);
+        const int nx = h->next;
+        h->amax[nx] = __uint_as_float(amax_bits);
+        h->next = (nx + 1) % FP8Q_HISTORY_LEN;
+        h->scale = s_u;
+        if (p.scale_out != nullptr) *p.scale_out = s_u;
+        __threadfence();
+        atomicExch(&h->arrivals, 0u);
+      }
+    }
+  }
+}
+
+// amax over a flat array: 16-byte loads, packed 16-bit max for bf16,
+// warp/CTA reduction, one atomicMax on the fp32 bit pattern per CTA (|x| bit
+// patterns order like the values; NaN patterns sort above Inf).
+template <typename InT>
+__global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, int64_t n,
+                                                   unsigned int *out) {
+  constexpr int kVec = 16 / sizeof(InT);
+  const int64_t nvec = n / kVec;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+  uint32_t m = 0;
+  auto upd = [&](uint4 w) {
+    if (sizeof(InT) == 2) {
+      m = __vmaxu2(m, w.x & 0x7FFF7FFFu);
+      m = __vmaxu2(m, w.y & 0x7FFF7FFFu);
+      m = __vmaxu2(m, w.z & 0x7FFF7FFFu);
+      m = __vmaxu2(m, w.w & 0x7FFF7FFFu);
+    } else {
+      m = max(m, w.x & 0x7FFFFFFFu);
+      m = max(m, w.y & 0x7FFFFFFFu);
+      m = max(m, w.z & 0x7FFFFFFFu);
+      m = max(m, w.w & 0x7FFFFFFFu);
+    }
+  };
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    uint4 w0 = __ldg(xv + i), w1 = __ldg(xv + i + stride), w2 = __ldg(xv + i + 2 * stride),
+          w3 = __ldg(xv + i + 3 * stride);
+    upd(w0); upd(w1); upd(w2); upd(w3);
+  }
+  for (; i < nvec; i += stride) upd(__ldg(xv + i));
+  if (sizeof(InT) == 2) m = max(m & 0xFFFFu, m >> 16) << 16;
+  // scalar tail (fewer than kVec elements)
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < n - nvec * kVec) {
+    const int64_t k = nvec * kVec + g;
+    uint32_t b;
+    if (sizeof(InT) == 2)
+      b = ((uint32_t) reinterpret_cast<const uint16_t *>(x)[k] << 16) & 0x7FFFFFFFu;
+    else
+      b = __float_as_uint(reinterpret_cast<const float *>(x)[k]) & 0x7FFFFFFFu;
+    m = max(m, b);
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  __shared__ uint32_t red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t r = red[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = max(r, red[w]);
+    atomicMax(out, r);
+  }
+}
+
+template <typename InT, int FMT, int KM>
+cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
+  static int blocks_per_sm = 0;
+  if (blocks_per_sm == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &blocks_per_sm, quant2d_kernel<InT, FMT, KM>, kQuantThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+  }
+  const int64_t ntiles = ((p.rows + 127) / 128) * ((p.cols + 127) / 128);
+  int64_t grid = (int64_t)sm_count() * blocks_per_sm;
+  if (ntiles < grid) grid = ntiles;
+  if (grid < 1) grid = 1;
+  quant2d_kernel<InT, FMT, KM><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename InT, int FMT>
+cudaError_t dispatch_mode(const QuantParams &p, cudaStream_t stream) {
+  switch (p.mode) {
+    case kModeTensorCurrent:
+      return launch_variant<InT, FMT, kKTensor>(p, stream);
+    case kModeTensorDelayed:
+      return launch_variant<InT, FMT, kKDelayed>(p, stream);
+    case kModeBlock:
+      return launch_variant<InT, FMT, kKBlock>(p, stream);
+    case kModeTile:
+      if (p.q != nullptr && p.q_t != nullptr) return launch_variant<InT, FMT, kKTileBoth>(p, stream);
+      if (p.q != nullptr) return launch_variant<InT, FMT, kKTileRow>(p, stream);
+      return launch_variant<InT, FMT, kKTileCol>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream) {
+  if (p.in_dtype == FP8Q_DT_BF16) {
+    return p.format == FP8Q_E4M3 ? dispatch_mode<uint16_t, FP8Q_E4M3>(p, stream)
+                                 : dispatch_mode<uint16_t, FP8Q_E5M2>(p, stream);
+  }
+  return p.format == FP8Q_E4M3 ? dispatch_mode<float, FP8Q_E4M3>(p, stream)
+                               : dispatch_mode<float, FP8Q_E5M2>(p, stream);
+}
+
+cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
+  if (e != cudaSuccess || n == 0) return e;
+  const int vec = in_dtype == FP8Q_DT_BF16 ? 8 : 4;
+  int64_t nvec = n / vec;
+  int64_t blocks = (nvec + 255) / 256;
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  unsigned int *out = reinterpret_cast<unsigned int *>(amax);
+  if (in_dtype == FP8Q_DT_BF16)
+    amax_kernel<uint16_t><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(x), n, out);
+  else
+    amax_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float *>(x), n, out);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8q

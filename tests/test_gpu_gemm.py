@@ -1,0 +1,297 @@
+"""GPU parity of steps a4-a5 (FP8 GEMM + epilogue) against the CPU oracle.
+
+The GEMM may round differently from the oracle's double sum, so each output
+must satisfy |y - y_ref| <= 2e-6 * sum_k |a_k b_k| + 1e-6, plus one bf16 ulp
+of y_ref for bf16 outputs.  Where every partial sum is exact in fp32 (small
+integers on a narrow exponent range) the GPU result must equal the oracle's
+exactly.  Operands come from the GPU quantize path and are first checked
+byte-exact against the oracle's own quantisation, so both sides multiply the
+same numbers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests.gpu_helpers import assert_bytes_equal, assert_f32_bits_equal, f32, to_oracle, u8
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fq():
+    import scaled_quantize_fp8_warp_gb300 as fq
+    from scaled_quantize_fp8_warp_gb300 import build_lib
+    build_lib.build()
+    fq.load_library()
+    assert fq.device_supported()
+    return fq
+
+
+def check_bound(got: np.ndarray, y_ref: np.ndarray, absum: np.ndarray, out_bf16: bool, what):
+    tol = oracle.gemm_bound(y_ref, absum, out_bf16)
+    err = np.abs(got.astype(np.float64) - y_ref)
+    bad = np.nonzero(~(err <= tol))
+    assert bad[0].size == 0, (f"{what}: {bad[0].size} outputs outside the bound; first at "
+                              f"{tuple(b[0] for b in bad)}: got {got[tuple(b[0] for b in bad)]}, "
+                              f"ref {y_ref[tuple(b[0] for b in bad)]}, "
+                              f"tol {tol[tuple(b[0] for b in bad)]}")
+
+
+def gpu_status_ok(fq):
+    assert fq.device_status() == 0, "a kernel reported a barrier timeout"
+
+
+# ----------------------------------------------------------- exact results
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (64, 64, 32), (300, 272, 512)])
+@pytest.mark.parametrize("fa,fb", [(0, 0), (1, 0), (0, 1)])
+def test_exact_small_integers(fq, M, N, K, fa, fb):
+    """Operands are FP8 codes of small integers (|v| <= 8) with scale 1:
+    every product and partial sum is an integer below 2^24, so the fp32
+    result is exact and must equal the oracle bit for bit."""
+    rng = np.random.default_rng(M + N + K + fa)
+    ints = np.arange(-8, 9, dtype=np.float32)
+    A = oracle.encode(rng.choice(ints, size=(M, K)), fa)
+    B = oracle.encode(rng.choice(ints, size=(N, K)), fb)
+    one = torch.ones(1, device="cuda")
+    opA = fq.GemmOperand.tensor(torch.from_numpy(A).cuda(), fa, one)
+    opB = fq.GemmOperand.tensor(torch.from_numpy(B).cuda(), fb, one)
+    y = fq.fp8_gemm(opA, opB, out_dtype=torch.float32)
+    gpu_status_ok(fq)
+    ref, _ = oracle.gemm_rows(oracle.GemmOperand.tensor(A, fa, 1.0),
+                              oracle.GemmOperand.tensor(B, fb, 1.0))
+    assert np.array_equal(f32(y).astype(np.float64), ref)
+
+
+def test_one_hot_columns(fq):
+    """B = identity-like one-hot rows: C[m, n] = A_deq[m, n] * B_deq[n, n]."""
+    M, N, K = 256, 128, 128
+    rng = np.random.default_rng(3)
+    A = oracle.encode(rng.standard_normal((M, K)).astype(np.float32) * 4, 0)
+    B = np.zeros((N, K), np.uint8)
+    B[np.arange(N), np.arange(N)] = 0x38            # 1.0
+    sa, sb = 0.75, 2.0
+    y = fq.fp8_gemm(fq.GemmOperand.tensor(torch.from_numpy(A).cuda(), 0,
+                                          torch.tensor([sa], device="cuda")),
+                    fq.GemmOperand.tensor(torch.from_numpy(B).cuda(), 0,
+                                          torch.tensor([sb], device="cuda")),
+                    out_dtype=torch.float32)
+    table = oracle.decode_table(0)
+    assert np.array_equal(f32(y), (table[A[:, :N]] * sa * sb).astype(np.float32))
+
+
+# ------------------------------------------------- tiny linear (fp32 out)
+
+def test_tiny_linear_all_roles(fq):
+    """x 512x32, w 64x32, g 512x64 (fp32), per-tensor current scaling, E4M3
+    forward and E5M2 gradient; fprop / dgrad / wgrad with fp32 output."""
+    x, w, g = workloads.tiny_linear()
+    xd, wd, gd = x.cuda(), w.cuda(), g.cuda()
+    qx, qxt, sx = fq.fp8_quantize_tensor(xd, 0, fq.fp8_amax(xd), want_qt=True)
+    qw, qwt, sw = fq.fp8_quantize_tensor(wd, 0, fq.fp8_amax(wd), want_qt=True)
+    qg, qgt, sg = fq.fp8_quantize_tensor(gd, 1, fq.fp8_amax(gd), want_qt=True)
+    rx, rxt, rsx = oracle.quantize_tensor(x.numpy(), 0, want_qt=True)
+    rw, rwt, rsw = oracle.quantize_tensor(w.numpy(), 0, want_qt=True)
+    rg, rgt, rsg = oracle.quantize_tensor(g.numpy(), 1, want_qt=True)
+    for got, ref, nm in [(qx, rx, "x"), (qxt, rxt, "x_t"), (qw, rw, "w"), (qwt, rwt, "w_t"),
+                         (qg, rg, "g"), (qgt, rgt, "g_t")]:
+        assert_bytes_equal(u8(got), ref, nm)
+    T = fq.GemmOperand.tensor
+    R = oracle.GemmOperand.tensor
+    y = fq.fp8_gemm_fprop(T(qx, 0, sx), T(qw, 0, sw), out_dtype=torch.float32)
+    dx = fq.fp8_gemm_dgrad(T(qg, 1, sg), T(qwt, 0, sw), out_dtype=torch.float32)
+    dw = fq.fp8_gemm_wgrad(T(qgt, 1, sg), T(qxt, 0, sx), out_dtype=torch.float32)
+    gpu_status_ok(fq)
+    assert y.shape == (512, 64) and dx.shape == (512, 32) and dw.shape == (64, 32)
+    for got, (yr, ab), nm in [
+        (y, oracle.gemm_rows(R(rx, 0, rsx), R(rw, 0, rsw)), "fprop"),
+        (dx, oracle.gemm_rows(R(rg, 1, rsg), R(rwt, 0, rsw)), "dgrad"),
+        (dw, oracle.gemm_rows(R(rgt, 1, rsg), R(rxt, 0, rsx)), "wgrad"),
+    ]:
+        check_bound(f32(got), yr, ab, False, nm)
+
+
+# --------------------------------------- per-tensor, ragged multi-tile shapes
+
+@pytest.mark.parametrize("M,N,K", [(300, 272, 400), (129, 512, 1024), (1000, 1040, 256),
+                                   (64, 16, 16), (257, 48, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_tensor_scaled_shapes(fq, M, N, K, out_dtype):
+    a = workloads.normal((M, K), 1.0, 40)
+    b = workloads.normal((N, K), 0.02, 41)
+    ad, bd = a.cuda(), b.cuda()
+    qa, _, sa = fq.fp8_quantize_tensor(ad, 0, fq.fp8_amax(ad))
+    qb, _, sb = fq.fp8_quantize_tensor(bd, 1, fq.fp8_amax(bd))
+    y = fq.fp8_gemm(fq.GemmOperand.tensor(qa, 0, sa), fq.GemmOperand.tensor(qb, 1, sb),
+                    out_dtype=out_dtype)
+    gpu_status_ok(fq)
+    ra, _, rsa = oracle.quantize_tensor(to_oracle(a), 0)
+    rb, _, rsb = oracle.quantize_tensor(to_oracle(b), 1)
+    assert_bytes_equal(u8(qa), ra, "A")
+    assert_bytes_equal(u8(qb), rb, "B")
+    yr, ab = oracle.gemm_rows(oracle.GemmOperand.tensor(ra, 0, rsa),
+                              oracle.GemmOperand.tensor(rb, 1, rsb))
+    check_bound(f32(y), yr, ab, out_dtype == torch.bfloat16, f"{M}x{N}x{K}")
+
+
+def test_k_zero_and_m_zero(fq):
+    one = torch.ones(1, device="cuda")
+    A = torch.zeros((64, 0), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((32, 0), dtype=torch.uint8, device="cuda")
+    y = fq.fp8_gemm(fq.GemmOperand.tensor(A, 0, one), fq.GemmOperand.tensor(B, 0, one),
+                    out_dtype=torch.float32)
+    assert torch.count_nonzero(y).item() == 0
+    A = torch.zeros((0, 32), dtype=torch.uint8, device="cuda")
+    B = torch.zeros((32, 32), dtype=torch.uint8, device="cuda")
+    y = fq.fp8_gemm(fq.GemmOperand.tensor(A, 0, one), fq.GemmOperand.tensor(B, 0, one))
+    assert y.shape == (0, 32)
+
+
+# ------------------------------------------- tile / block scaled (promoted)
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 512), (300, 272, 400), (1000, 1040, 384),
+                                   (128, 512, 128), (200, 48, 1040)])
+@pytest.mark.parametrize("b_kind", ["block", "tile"])
+def test_block_scaled_shapes(fq, M, N, K, b_kind):
+    a, _ = workloads.with_outlier_rows((M, K), 1.0, 0.05, 50.0, 50)
+    b = workloads.normal((N, K), 0.02, 51)
+    b[:, : min(K, 128)] *= 30                        # scale differences across K blocks
+    ad, bd = a.cuda(), b.cuda()
+    qa, sa, _, _ = fq.fp8_quantize_tile1x128(ad, 0, rows=True)
+    ra, rsa = oracle.quantize_tile_rows(to_oracle(a), 0)
+    assert_bytes_equal(u8(qa), ra, "A")
+    assert_f32_bits_equal(f32(sa), rsa, "A scales")
+    if b_kind == "block":
+        qb, _, sb = fq.fp8_quantize_block128x128(bd, 1)
+        rb, _, rsb = oracle.quantize_block(to_oracle(b), 1)
+        opB, ropB = fq.GemmOperand.block(qb, 1, sb), oracle.GemmOperand.block(rb, 1, rsb)
+    else:
+        qb, sb, _, _ = fq.fp8_quantize_tile1x128(bd, 1, rows=True)
+        rb, rsb = oracle.quantize_tile_rows(to_oracle(b), 1)
+        opB, ropB = fq.GemmOperand.tile(qb, 1, sb), oracle.GemmOperand.tile(rb, 1, rsb)
+    assert_bytes_equal(u8(qb), rb, "B")
+    y = fq.fp8_gemm(fq.GemmOperand.tile(qa, 0, sa), opB, out_dtype=torch.bfloat16)
+    gpu_status_ok(fq)
+    yr, ab = oracle.gemm_rows(oracle.GemmOperand.tile(ra, 0, rsa), ropB)
+    check_bound(f32(y), yr, ab, True, f"{b_kind} {M}x{N}x{K}")
+
+
+def test_block_scaled_transposed_weight_scales(fq):
+    """Dgrad's B operand is w^T with the weight's block scales read
+    transposed (stride_row = 1, stride_k = ceil(K/128))."""
+    M, N, K = 384, 256, 640         # layer sizes: g [M, N], w [N, K]
+    g = workloads.normal((M, N), 1e-3, 60)
+    w = workloads.normal((N, K), 0.02, 61)
+    qg, sg, _, _ = fq.fp8_quantize_tile1x128(g.cuda(), 1, rows=True)
+    _, qwt, sw = fq.fp8_quantize_block128x128(w.cuda(), 0, want_q=False, want_qt=True)
+    dx = fq.fp8_gemm_dgrad(fq.GemmOperand.tile(qg, 1, sg),
+                           fq.GemmOperand.block_transposed(qwt, 0, sw))
+    gpu_status_ok(fq)
+    rg, rsg = oracle.quantize_tile_rows(to_oracle(g), 1)
+    _, rwt, rsw = oracle.quantize_block(to_oracle(w), 0, want_q=False, want_qt=True)
+    assert_bytes_equal(u8(qwt), rwt, "w_t")
+    yr, ab = oracle.gemm_rows(oracle.GemmOperand.tile(rg, 1, rsg),
+                              oracle.GemmOperand.block(rwt, 0, rsw, transposed=True))
+    check_bound(f32(dx), yr, ab, True, "dgrad")
+
+
+# ---------------------------------------------- full-size layer, sampled
+
+def _sample_points(M, N, rng, n=4096):
+    ms = rng.integers(0, M, n)
+    ns = rng.integers(0, N, n)
+    # plus whole 128x128 tiles at two corners and the middle
+    tiles = []
+    for m0, n0 in [(0, 0), (M - 128, N - 128), ((M // 256) * 128, (N // 256) * 128)]:
+        mm, nn = np.meshgrid(np.arange(m0, m0 + 128), np.arange(n0, n0 + 128), indexing="ij")
+        tiles.append((mm.ravel(), nn.ravel()))
+    ms = np.concatenate([ms] + [t[0] for t in tiles])
+    ns = np.concatenate([ns] + [t[1] for t in tiles])
+    return ms, ns
+
+
+@pytest.mark.parametrize("layer", [0, 1])      # QKV, attention out
+def test_layer_fprop_full_size_tensor(fq, layer):
+    shape = workloads.LAYER[layer]
+    x, w, _ = workloads.layer_inputs(shape, layer)
+    M, K, N = x.shape[0], shape.K, shape.N
+    xd, wd = x.cuda(), w.cuda()
+    qx, _, sx = fq.fp8_quantize_tensor(xd, 0, fq.fp8_amax(xd))
+    qw, _, sw = fq.fp8_quantize_tensor(wd, 0, fq.fp8_amax(wd))
+    y = fq.fp8_gemm_fprop(fq.GemmOperand.tensor(qx, 0, sx), fq.GemmOperand.tensor(qw, 0, sw))
+    gpu_status_ok(fq)
+    rx, _, rsx = oracle.quantize_tensor(to_oracle(x), 0)
+    rw, _, rsw = oracle.quantize_tensor(to_oracle(w), 0)
+    assert_bytes_equal(u8(qx), rx, "x")
+    assert_bytes_equal(u8(qw), rw, "w")
+    ms, ns = _sample_points(M, N, np.random.default_rng(layer))
+    yr, ab = oracle.gemm_points(oracle.GemmOperand.tensor(rx, 0, rsx),
+                                oracle.GemmOperand.tensor(rw, 0, rsw), ms, ns)
+    check_bound(f32(y)[ms, ns], yr, ab, True, f"{shape.name} fprop")
+
+
+def test_layer_all_roles_full_size_block(fq):
+    """Attention-out layer at full size with 1x128 / 128x128 scaling: fprop,
+    dgrad (B = w^T, transposed block scales) and wgrad (column tiles of g and
+    x), each sampled against the oracle."""
+    idx = 1
+    shape = workloads.LAYER[idx]
+    x, w, g = workloads.layer_inputs(shape, idx)
+    M, K, N = x.shape[0], shape.K, shape.N
+    xd, wd, gd = x.cuda(), w.cuda(), g.cuda()
+    qx, sx, qxt, sxt = fq.fp8_quantize_tile1x128(xd, 0, rows=True, cols=True)
+    qw, qwt, sw = fq.fp8_quantize_block128x128(wd, 0, want_q=True, want_qt=True)
+    qg, sg, qgt, sgt = fq.fp8_quantize_tile1x128(gd, 1, rows=True, cols=True)
+    T, B, BT = fq.GemmOperand.tile, fq.GemmOperand.block, fq.GemmOperand.block_transposed
+    y = fq.fp8_gemm_fprop(T(qx, 0, sx), B(qw, 0, sw))
+    dx = fq.fp8_gemm_dgrad(T(qg, 1, sg), BT(qwt, 0, sw))
+    dw = fq.fp8_gemm_wgrad(T(qgt, 1, sgt), T(qxt, 0, sxt))
+    gpu_status_ok(fq)
+    xo, wo, go = to_oracle(x), to_oracle(w), to_oracle(g)
+    rx, rsx = oracle.quantize_tile_rows(xo, 0)
+    rxt, rsxt = oracle.quantize_tile_cols(xo, 0)
+    rw, rwt, rsw = oracle.quantize_block(wo, 0, want_qt=True)
+    rg, rsg = oracle.quantize_tile_rows(go, 1)
+    rgt, rsgt = oracle.quantize_tile_cols(go, 1)
+    for got, ref, nm in [(qx, rx, "x"), (qxt, rxt, "x_t"), (qw, rw, "w"), (qwt, rwt, "w_t"),
+                         (qg, rg, "g"), (qgt, rgt, "g_t")]:
+        assert_bytes_equal(u8(got), ref, nm)
+    for got, ref, nm in [(sx, rsx, "sx"), (sxt, rsxt, "sxt"), (sw, rsw, "sw"), (sg, rsg, "sg"),
+                         (sgt, rsgt, "sgt")]:
+        assert_f32_bits_equal(f32(got), ref, nm)
+    RT, RB = oracle.GemmOperand.tile, oracle.GemmOperand.block
+    rng = np.random.default_rng(9)
+    cases = [
+        (y, RT(rx, 0, rsx), RB(rw, 0, rsw), M, N, "fprop"),
+        (dx, RT(rg, 1, rsg), RB(rwt, 0, rsw, transposed=True), M, K, "dgrad"),
+        (dw, RT(rgt, 1, rsgt), RT(rxt, 0, rsxt), N, K, "wgrad"),
+    ]
+    for got, opA, opB, R, C, nm in cases:
+        ms, ns = _sample_points(R, C, rng, n=2048)
+        yr, ab = oracle.gemm_points(opA, opB, ms, ns)
+        check_bound(f32(got)[ms, ns], yr, ab, True, nm)
+
+
+def test_linear_autocast_matches_steps(fq):
+    """fp8_linear_autocast equals the same steps called one by one."""
+    M, N, K = 512, 384, 256
+    x = workloads.normal((M, K), 1.0, 70).cuda()
+    w = workloads.normal((N, K), 0.02, 71).cuda()
+    for recipe in (fq.RECIPE_TENSOR_CURRENT, fq.RECIPE_BLOCK):
+        y = fq.fp8_linear_autocast(x, w, recipe=recipe)
+        if recipe == fq.RECIPE_TENSOR_CURRENT:
+            qx, _, sx = fq.fp8_quantize_tensor(x, 0, fq.fp8_amax(x))
+            qw, _, sw = fq.fp8_quantize_tensor(w, 0, fq.fp8_amax(w))
+            y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tensor(qx, 0, sx),
+                                   fq.GemmOperand.tensor(qw, 0, sw))
+        else:
+            qx, sx, _, _ = fq.fp8_quantize_tile1x128(x, 0)
+            qw, _, sw = fq.fp8_quantize_block128x128(w, 0)
+            y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tile(qx, 0, sx), fq.GemmOperand.block(qw, 0, sw))
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    hx, hw = fq.History(initial=[3.0] * 16), fq.History(initial=[0.05] * 16)
+    y = fq.fp8_linear_autocast(x, w, recipe=fq.RECIPE_TENSOR_DELAYED, hist_x=hx, hist_w=hw)
+    gpu_status_ok(fq)
+    assert torch.isfinite(y.float()).all()

@@ -149,9 +149,15 @@ float orc_scale_from_amax(float amax, int fmt) {
 /* ------------------------------------------------------------------- casts */
 
 /* q = (x / scale).to(fp8) ([fp8_parity] scaled_roundtrip): an fp32 IEEE
- * division, then one round-to-nearest-even into the format. */
+ * division, then one round-to-nearest-even into the format.
+ * NaN (the pages never meet one; IEEE 754 leaves the sign of a NaN result
+ * open and x86 and aarch64 disagree on it): a NaN input keeps its sign, as
+ * the plain cast does (0x7F | sign); a NaN that the division itself creates
+ * (NaN scale, Inf / Inf) is encoded 0x7F. */
 static uint8_t cast_one(float xv, float s, int fmt, int saturate) {
+  if (isnan(xv)) return (uint8_t)(0x7F | (signbit(xv) ? 0x80 : 0x00));
   float v = xv / s;
+  if (isnan(v)) return 0x7F;
   return orc_fp8_encode(v, fmt, saturate);
 }
 

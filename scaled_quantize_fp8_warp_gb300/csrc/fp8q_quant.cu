@@ -99,11 +99,22 @@ __device__ __forceinline__ uint2 cast8_fast(const float (&v)[8], float s, float 
   return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
 }
 
+// Slow path per element: a NaN input keeps its sign (0x7F | sign); a NaN the
+// division creates (NaN scale, Inf / Inf) is 0x7F; everything else is the
+// IEEE quotient under the full encode rules.
+template <int FMT>
+__device__ __forceinline__ uint32_t cast1_slow(float x, float s, int saturate) {
+  if (x != x) return 0x7Fu | ((__float_as_uint(x) >> 24) & 0x80u);
+  const float v = __fdiv_rn(x, s);
+  if (v != v) return 0x7Fu;
+  return encode_slow<FMT>(v, saturate);
+}
+
 template <int FMT>
 __device__ __noinline__ uint2 cast8_slow(const float (&v)[8], float s, int saturate) {
   uint32_t b[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = encode_slow<FMT>(__fdiv_rn(v[j], s), saturate);
+  for (int j = 0; j < 8; ++j) b[j] = cast1_slow<FMT>(v[j], s, saturate);
   return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
                     b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
 }

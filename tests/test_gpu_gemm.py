@@ -291,7 +291,17 @@ def test_linear_autocast_matches_steps(fq):
             qw, _, sw = fq.fp8_quantize_block128x128(w, 0)
             y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tile(qx, 0, sx), fq.GemmOperand.block(qw, 0, sw))
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
-    hx, hw = fq.History(initial=[3.0] * 16), fq.History(initial=[0.05] * 16)
+    # histories that cover the data (x ~ N(0,1), w ~ N(0,0.02)) keep every
+    # quotient in range; the result then equals per-tensor casts with the
+    # history scales
+    hx, hw = fq.History(initial=[6.0] * 16), fq.History(initial=[0.12] * 16)
     y = fq.fp8_linear_autocast(x, w, recipe=fq.RECIPE_TENSOR_DELAYED, hist_x=hx, hist_w=hw)
     gpu_status_ok(fq)
     assert torch.isfinite(y.float()).all()
+    sx = torch.tensor([6.0 / 448.0], device="cuda")
+    sw = torch.tensor([0.12 / 448.0], device="cuda")
+    qx, _, _ = fq.fp8_quantize_tensor(x, 0, sx * 448.0)
+    qw, _, _ = fq.fp8_quantize_tensor(w, 0, sw * 448.0)
+    y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tensor(qx, 0, sx), fq.GemmOperand.tensor(qw, 0, sw))
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert hx.state()[1] == 1 and hw.state()[1] == 1

@@ -48,7 +48,68 @@ def parse_args():
     ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip timing the oracle on the host cores")
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES),
+                    help="run one kernel on a small case three times for an ncu capture "
+                         "(prints no bench line)")
     return ap.parse_args()
+
+
+# Small cases for ncu captures: operands about L2-sized or larger, a few
+# hundred MB on the device, three launches of the kernel under study.
+PROFILE_CASES = {
+    "gemm_tensor": "8192x8192x8192 per-tensor E4M3 GEMM, bf16 out",
+    "gemm_block": "8192x8192x8192 1x128 x 128x128 GEMM, bf16 out",
+    "gemm_tile": "8192x8192x8192 1x128 x 1x128 GEMM (wgrad form), bf16 out",
+    "quant_tile_dual": "16384x8192 bf16, 1x128 row and column tiles, E4M3",
+    "quant_tile_rows": "16384x8192 bf16, 1x128 row tiles, E4M3",
+    "quant_block": "16384x8192 bf16, 128x128 blocks + transposed copy, E4M3",
+    "amax": "16384x8192 bf16 amax",
+}
+
+
+def run_profile_case(case: str):
+    import torch
+    import scaled_quantize_fp8_warp_gb300 as fq
+    from scaled_quantize_fp8_warp_gb300 import build_lib
+    import workloads
+    build_lib.build()
+    fq.load_library()
+    if case.startswith("gemm"):
+        M = N = K = 8192
+        a = workloads.normal((M, K), 1.0, 900).cuda()
+        b = workloads.normal((N, K), 0.02, 901).cuda()
+        if case == "gemm_tensor":
+            qa, _, sa = fq.fp8_quantize_tensor(a, fq.E4M3, fq.fp8_amax(a))
+            qb, _, sb = fq.fp8_quantize_tensor(b, fq.E4M3, fq.fp8_amax(b))
+            A, B = fq.GemmOperand.tensor(qa, 0, sa), fq.GemmOperand.tensor(qb, 0, sb)
+        else:
+            qa, sa, _, _ = fq.fp8_quantize_tile1x128(a, fq.E4M3)
+            A = fq.GemmOperand.tile(qa, 0, sa)
+            if case == "gemm_block":
+                qb, _, sb = fq.fp8_quantize_block128x128(b, fq.E4M3)
+                B = fq.GemmOperand.block(qb, 0, sb)
+            else:
+                qb, sb, _, _ = fq.fp8_quantize_tile1x128(b, fq.E4M3)
+                B = fq.GemmOperand.tile(qb, 0, sb)
+        del a, b
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            fq.fp8_gemm(A, B, out=out)
+    else:
+        x = workloads.normal((16384, 8192), 1.0, 902).cuda()
+        for _ in range(3):
+            if case == "quant_tile_dual":
+                fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True, cols=True)
+            elif case == "quant_tile_rows":
+                fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True)
+            elif case == "quant_block":
+                fq.fp8_quantize_block128x128(x, fq.E4M3, want_q=True, want_qt=True)
+            else:
+                fq.fp8_amax(x)
+    torch.cuda.synchronize()
+    if fq.device_status() != 0:
+        raise SystemExit("profile case: a kernel reported a barrier timeout")
+    print(f"profile case {case} done: {PROFILE_CASES[case]}")
 
 
 def load_peaks():
@@ -485,6 +546,9 @@ def layer_config():
 
 def main():
     args = parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case)
+        return
     dist = Dist()
     if args.impl == "reference":
         run_reference(args, dist)
@@ -554,9 +618,16 @@ def main():
     R, C = xq.shape
     n = R * C
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=xq.device)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=xq.device)
 
     def flush():
-        flush_buf.fill_(1.0)
+        # write a buffer twice the size of L2, then read it back so the lines
+        # left in L2 are clean (no write-backs charged to the timed kernel);
+        # on the timed stream, finished before the start event
+        with torch.cuda.stream(stream):
+            flush_buf.fill_(1.0)
+            torch.sum(flush_buf, out=flush_sink)
+        torch.cuda.synchronize()
 
     qt = torch.empty((R, C), dtype=torch.uint8, device=xq.device)
     st = torch.empty(((C + 127) // 128, R), dtype=torch.float32, device=xq.device)

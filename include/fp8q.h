@@ -144,7 +144,8 @@ int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax,
  *   scale_out  device float or NULL: receives s
  *   q          device [rows, cols] FP8 bytes or NULL
  *   q_t        device [cols, rows] FP8 bytes (the transpose) or NULL;
- *              requires rows % 16 == 0.  At least one of q, q_t non-NULL.
+ *              requires rows % 16 == 0.  At least one of q, q_t non-NULL
+ *              unless the matrix is empty (then only *scale_out is written).
  * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
 int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows,
                         int64_t cols, int format, const float *amax,

@@ -179,7 +179,8 @@ int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows, int64_t cols,
                         int saturate, cudaStream_t stream) {
   int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
   if (rc != FP8Q_OK) return rc;
-  if (amax == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if (amax == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && q == nullptr && q_t == nullptr) return FP8Q_ERR_INVALID_ARG;
   if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
   if ((rc = check_device()) != FP8Q_OK) return rc;
   QuantParams p{};
@@ -205,7 +206,8 @@ int fp8_quantize_delayed(const void *x, int in_dtype, int64_t rows, int64_t cols
                          int saturate, cudaStream_t stream) {
   int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
   if (rc != FP8Q_OK) return rc;
-  if (hist == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if (hist == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && q == nullptr && q_t == nullptr) return FP8Q_ERR_INVALID_ARG;
   if ((rc = check_ptr(hist, true)) != FP8Q_OK) return rc;
   if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
   if ((rc = check_device()) != FP8Q_OK) return rc;
@@ -244,9 +246,11 @@ int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows, int64_t co
   const bool want_col = q_t != nullptr || qt_scales != nullptr;
   int rc = check_quant(x, in_dtype, rows, cols, format, want_col);
   if (rc != FP8Q_OK) return rc;
-  if (!want_row && !want_col) return FP8Q_ERR_INVALID_ARG;
-  if (want_row && (q == nullptr || q_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
-  if (want_col && (q_t == nullptr || qt_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0) {
+    if (!want_row && !want_col) return FP8Q_ERR_INVALID_ARG;
+    if (want_row && (q == nullptr || q_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+    if (want_col && (q_t == nullptr || qt_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  }
   if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
   if ((q_scales && (reinterpret_cast<uintptr_t>(q_scales) & 3u)) ||
       (qt_scales && (reinterpret_cast<uintptr_t>(qt_scales) & 3u)))
@@ -276,7 +280,8 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t
                               int saturate, cudaStream_t stream) {
   int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
   if (rc != FP8Q_OK) return rc;
-  if (block_scales == nullptr || (q == nullptr && q_t == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (block_scales == nullptr || (q == nullptr && q_t == nullptr)))
+    return FP8Q_ERR_INVALID_ARG;
   if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
   if (reinterpret_cast<uintptr_t>(block_scales) & 3u) return FP8Q_ERR_MISALIGNED;
   if ((rc = check_device()) != FP8Q_OK) return rc;

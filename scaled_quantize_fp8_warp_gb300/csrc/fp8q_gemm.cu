@@ -321,7 +321,17 @@ __global__ void __launch_bounds__(192, 1)
 // ------------------------------------------------------------------------
 constexpr int kBSBN = 256;
 constexpr int kBSStages = 4;
-constexpr int kBSThreads = 384;  // 168 registers per thread at one CTA per SM
+constexpr int kBSThreads = 384;
+// Register split (setmaxnreg, inside each role's branch): the 384-thread launch
+// gets 168 registers per thread (65536 / 384 rounded down to 8); warpgroup 0
+// (producer, MMA, two idle warps) drops to 40, the two promotion warpgroups
+// rise to 232: 128 * 40 + 256 * 232 = 64512 = 384 * 168.  The host checks
+// the compiled launch count before the first launch.
+constexpr int kBSLaunchRegs = 168;
+constexpr int kBSLowRegs = 40;
+constexpr int kBSHighRegs = 232;
+static_assert(128 * kBSLowRegs + 256 * kBSHighRegs <= kBSThreads * kBSLaunchRegs,
+              "register split exceeds the launch allocation");
 
 template <bool B_TILE, bool OUT_BF16>
 __global__ void __launch_bounds__(kBSThreads, 1)
@@ -371,10 +381,12 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   const int total = p.num_m_tiles * p.num_n_tiles;
   const int nkb = p.num_k_blocks;
 
-  if (warp == 0) {
-    if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
-    __syncwarp();
-  } else if (warp == 1) {
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBSLowRegs));
+    if (warp == 0) {
+      if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
+      __syncwarp();
+    } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
@@ -396,7 +408,9 @@ __global__ void __launch_bounds__(kBSThreads, 1)
       drain_mma(drain, abort_flag);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBSHighRegs));
     // Promotion warps 4..11: warpgroup wg owns tile columns [128 wg, 128 wg + 128);
     // TMEM lane quarter = warp % 4.  Scales for K block kb + 1 are fetched
     // into registers while block kb is promoted; B tile scales go through a
@@ -460,25 +474,34 @@ __global__ void __launch_bounds__(kBSThreads, 1)
         tc_fence_after();
         const float sab = __fmul_rn(sa, sb);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(
-              tmem_base + ((uint32_t)(quarter * 32) << 16) + pb * BN + wg * 128 + c * 16, r);
+        for (int h = 0; h < 2; ++h) {
+          // 64 columns per round trip: two 32-column TMEM loads, one wait
+          uint32_t r0[32], r1[32];
+          const uint32_t col = pb * BN + wg * 128 + h * 64;
+          const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+          tmem_ld_32x32b_x32(tmem_base + lane_base + col, r0);
+          tmem_ld_32x32b_x32(tmem_base + lane_base + col + 32, r1);
           tmem_ld_wait();
-          if (c == 7) {
+          if (h == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pe0 + 8 * pb);
           }
           if (B_TILE) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[c * 16 + j] = __fmaf_rn(__uint_as_float(r[j]), __fmul_rn(sa, my_bs[c * 16 + j]),
-                                          acc[c * 16 + j]);
+            for (int j = 0; j < 32; ++j) {
+              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]),
+                                          __fmul_rn(sa, my_bs[h * 64 + j]), acc[h * 64 + j]);
+              acc[h * 64 + 32 + j] =
+                  __fmaf_rn(__uint_as_float(r1[j]), __fmul_rn(sa, my_bs[h * 64 + 32 + j]),
+                            acc[h * 64 + 32 + j]);
+            }
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[c * 16 + j] = __fmaf_rn(__uint_as_float(r[j]), sab, acc[c * 16 + j]);
+            for (int j = 0; j < 32; ++j) {
+              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[h * 64 + j]);
+              acc[h * 64 + 32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[h * 64 + 32 + j]);
+            }
           }
         }
       }
@@ -562,6 +585,11 @@ int run_blockscaled(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs
   auto kernel = gemm_blockscaled_kernel<B_TILE, OUT_BF16>;
   static bool attr_done = false;
   if (!attr_done) {
+    // The setmaxnreg split is only safe if the kernel launches with at least
+    // kBSLaunchRegs registers per thread; refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (fa.numRegs < kBSLaunchRegs) return FP8Q_ERR_CUDA;
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
     attr_done = true;
   }

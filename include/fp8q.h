@@ -281,6 +281,39 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M,
                         void *y, int out_dtype, void *workspace,
                         size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------ forward without a workspace */
+
+/* Size of the static scratch used by fp8_linear_autocast_noalloc. */
+#define FP8Q_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* fp8_linear_autocast for callers that cannot call cudaMalloc: for example a
+ * plugin hosted by an application that owns all device memory and passes in
+ * only the tensors, a serving loop that forbids allocation after start-up, or
+ * code under another allocator's accounting that may not grow the device
+ * footprint.  Such callers cannot provide the workspace fp8_linear_autocast
+ * needs, so this variant keeps it in one file-scope device array of
+ * FP8Q_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library.  The source pages
+ * have no counterpart to this entry point.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *     routine.  Every GPU on which the library's device code is loaded holds
+ *     the 64 MiB array until the process exits.
+ *   - Sizes whose scratch, fp8q_linear_workspace_size(recipe, M, N, K),
+ *     exceeds FP8Q_NOALLOC_SCRATCH_BYTES are rejected with
+ *     FP8Q_ERR_WORKSPACE before any device work.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one array, which keeps the last call's
+ *     contents.  Each call clears what must start at zero (the amax words)
+ *     itself.  Calls whose work overlaps on the GPU (other streams, other
+ *     host threads) race on the array: serialise them.
+ * Arguments, results and the other errors are those of fp8_linear_autocast. */
+int fp8_linear_autocast_noalloc(const void *x, const void *w, int in_dtype,
+                                int64_t M, int64_t N, int64_t K, int recipe,
+                                fp8q_amax_history *hist_x,
+                                fp8q_amax_history *hist_w, void *y,
+                                int out_dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

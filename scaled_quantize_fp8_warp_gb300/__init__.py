@@ -46,6 +46,7 @@ EXPORTS = (
     "fp8_quantize_tensor", "fp8_quantize_delayed", "fp8q_history_init",
     "fp8_quantize_tile1x128", "fp8_quantize_block128x128", "fp8_gemm", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
+    "fp8_linear_autocast_noalloc",
 )
 
 
@@ -96,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8q_linear_workspace_size": (SZ, [I32, I64, I64, I64]),
             "fp8_linear_autocast": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32, P, SZ,
                                           P]),
+            "fp8_linear_autocast_noalloc": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32,
+                                                  P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -357,6 +360,27 @@ def fp8_linear_autocast(x, w, recipe=RECIPE_TENSOR_CURRENT, out_dtype=torch.bflo
         _ptr(hist_x.buf) if hist_x else None, _ptr(hist_w.buf) if hist_w else None,
         _ptr(out), _out_dtype(out.dtype), _ptr(workspace), workspace.numel(), _stream(stream)),
         "fp8_linear_autocast")
+    return out
+
+
+#: size of the library's static scratch (FP8Q_NOALLOC_SCRATCH_BYTES)
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def fp8_linear_autocast_noalloc(x, w, recipe=RECIPE_TENSOR_CURRENT, out_dtype=torch.bfloat16,
+                                hist_x: History | None = None, hist_w: History | None = None,
+                                out=None, stream=None):
+    """fp8_linear_autocast for callers that cannot allocate device memory:
+    the library keeps the FP8 copies and scales in its own fixed 64 MiB
+    device array (see include/fp8q.h), so only the output is supplied here.
+    Pass ``out`` to make the call allocate nothing at all from Python either."""
+    M, K = _rows_cols(x)
+    N = w.shape[0]
+    out = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=x.device)
+    _check(lib().fp8_linear_autocast_noalloc(
+        _ptr(x), _ptr(w), _in_dtype(x), M, N, K, recipe,
+        _ptr(hist_x.buf) if hist_x else None, _ptr(hist_w.buf) if hist_w else None,
+        _ptr(out), _out_dtype(out.dtype), _stream(stream)), "fp8_linear_autocast_noalloc")
     return out
 
 

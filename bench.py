@@ -5,17 +5,18 @@
 
 One step is one pass of the whole path over one layer's synthetic inputs:
 the 12 GEMMs (Fprop / Dgrad / Wgrad of QKV, attention out, MLP up, MLP down;
-M = 31 x 512 = 15872 tokens, hidden 4096, FFN 16384) with 1x128 tile scaling
-of activations and gradients and 128x128 block scaling of weights, in
-autocast mode: every step quantises x (row and column tiles), w (blocks and
-the transposed copy) and grad_out (row and column tiles) before its GEMMs,
-as the low-precision-training blog post's autocast timing does.  The
+M = 31 x 512 = 15872 tokens, hidden 4096, FFN 16384) with per-tensor current
+scaling, in autocast mode: every step takes the amax of x, w and grad_out,
+derives their scales and casts them (E4M3 / E5M2, each with its transposed
+copy for the backward GEMMs) before the GEMMs, as the low-precision-training
+blog post's autocast timing does for its FP8 CurrentScaling recipe.  The
 headline value is whole-job TFLOP/s of that step (2 M N K summed over the 12
 GEMMs / step time).  The same line also reports the prequantized step (GEMM
-kernels only), the per-tensor current and delayed recipes, quantize GB/s on
-the 8192x4096 activation, the dominant kernel's roofline, an end-to-end
-figure with host buffers, the oracle timed on the host cores, and SM clocks
-sampled during the timed region.
+kernels only), delayed scaling of the gradient, the same layer with 1x128 /
+128x128 block scaling (autocast and prequant), quantize GB/s on the
+8192x4096 activation, the dominant kernels' rooflines, an end-to-end figure
+with host buffers, the oracle timed on the host cores, and SM clocks sampled
+during the timed region.
 
 Under torchrun each rank runs an independent replica of the step on its own
 GPU (no data-path collective; weak scaling); timings are maxed over ranks.
@@ -381,18 +382,20 @@ class Runner:
             for role in ("fprop", "dgrad", "wgrad"):
                 self._gemm(role, *o[role])
 
+    tensor_autocast.launches = 4 * 9   # per linear: 3 amax, 3 casts, 3 GEMMs
+
     def tensor_prequant(self):
         self.gemms(self.tops)
 
     # end to end: host inputs in, host outputs out --------------------------
-    def e2e_block(self):
+    def e2e_tensor(self):
         st = self.stream
         with self.torch.cuda.stream(st):
             for L in self.s.linears:
                 L["x"].copy_(L["x_h"], non_blocking=True)
                 L["w"].copy_(L["w_h"], non_blocking=True)
                 L["g"].copy_(L["g_h"], non_blocking=True)
-        self.block_autocast()
+        self.tensor_autocast(False)
         with self.torch.cuda.stream(st):
             for L in self.s.linears:
                 L["y_h"].copy_(L["y"], non_blocking=True)
@@ -438,53 +441,62 @@ def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None):
 
 # ------------------------------------------------------------- CPU baseline
 
-def oracle_layer_sample(rows: int, threads: int):
+class OracleLayerSample:
     """The oracle on a bounded sample of the block-scaled layer step: for
-    each of the 12 GEMMs, `rows` output rows x one 128-row block of B: the
-    oracle quantises those A rows and that B block (1x128 tiles / 128x128
-    blocks) and computes the double-accumulated GEMM.  Returns (flops, s)."""
-    import concurrent.futures as cf
+    each of the 12 GEMMs, `rows` output rows x one 128-row block of B.  The
+    inputs are drawn once; each run() quantises those A rows and that B block
+    with the oracle (1x128 tiles / 128x128 blocks) and computes the
+    double-accumulated GEMM, spread over `threads` host threads (the oracle is
+    plain C; ctypes releases the GIL).  run() returns (flops, seconds)."""
 
-    import numpy as np
-    import torch
+    def __init__(self, rows: int, threads: int):
+        import numpy as np
+        import torch
 
-    import oracle
-    import workloads
+        import workloads
 
-    def bits(t):
-        return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+        def bits(t):
+            return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
 
-    jobs = []
-    for i, shape in enumerate(workloads.LAYER):
-        x, w, g = workloads.layer_inputs(shape, i)
-        # fprop: A = x rows (1x128), B = w rows 0..127 (block)
-        jobs.append(("fprop", bits(x[:rows]), bits(w[:128]), 0, 0, "block"))
-        # dgrad: A = g rows (1x128, E5M2), B = w^T rows 0..127 (block of w^T)
-        jobs.append(("dgrad", bits(g[:rows]), bits(w[:, :128].t()), 1, 0, "block"))
-        # wgrad: A = g^T rows (column tiles of g), B = x^T rows 0..127 (column tiles of x)
-        jobs.append(("wgrad", bits(g[:, :rows].t()), bits(x[:, :128].t()), 1, 0, "tile"))
-    pool = cf.ThreadPoolExecutor(max_workers=threads)
+        self.rows, self.threads = rows, threads
+        self.jobs = []
+        for i, shape in enumerate(workloads.LAYER):
+            x, w, g = workloads.layer_inputs(shape, i)
+            # fprop: A = x rows (1x128), B = w rows 0..127 (block)
+            self.jobs.append((bits(x[:rows]), bits(w[:128]), 0, 0, "block"))
+            # dgrad: A = g rows (1x128, E5M2), B = rows 0..127 of w^T (block)
+            self.jobs.append((bits(g[:rows]), bits(w[:, :128].t()), 1, 0, "block"))
+            # wgrad: A = rows of g^T (column tiles of g), B = rows of x^T
+            self.jobs.append((bits(g[:, :rows].t()), bits(x[:, :128].t()), 1, 0, "tile"))
 
-    def run(job):
-        _, a, b, fa, fb, bkind = job
-        qa, sa = oracle.quantize_tile_rows(a, fa)
-        A = oracle.GemmOperand.tile(qa, fa, sa)
-        if bkind == "block":
-            qb, _, sb = oracle.quantize_block(b, fb)
-            B = oracle.GemmOperand.block(qb, fb, sb)
-        else:
-            qb, sb = oracle.quantize_tile_rows(b, fb)
-            B = oracle.GemmOperand.tile(qb, fb, sb)
-        step = max(1, a.shape[0] // 4)
-        parts = [(m0, min(a.shape[0], m0 + step)) for m0 in range(0, a.shape[0], step)]
-        list(pool.map(lambda p: oracle.gemm_rows(A, B, p[0], p[1]), parts))
-        return 2.0 * a.shape[0] * b.shape[0] * a.shape[1]
+    def run(self):
+        import concurrent.futures as cf
 
-    t0 = time.perf_counter()
-    flops = sum(cf.ThreadPoolExecutor(max_workers=max(1, threads // 4)).map(run, jobs))
-    dt = time.perf_counter() - t0
-    pool.shutdown()
-    return flops, dt
+        import oracle
+
+        pool = cf.ThreadPoolExecutor(max_workers=self.threads)
+
+        def one(job):
+            a, b, fa, fb, bkind = job
+            qa, sa = oracle.quantize_tile_rows(a, fa)
+            A = oracle.GemmOperand.tile(qa, fa, sa)
+            if bkind == "block":
+                qb, _, sb = oracle.quantize_block(b, fb)
+                B = oracle.GemmOperand.block(qb, fb, sb)
+            else:
+                qb, sb = oracle.quantize_tile_rows(b, fb)
+                B = oracle.GemmOperand.tile(qb, fb, sb)
+            step = max(1, a.shape[0] // 8)
+            parts = [(m0, min(a.shape[0], m0 + step)) for m0 in range(0, a.shape[0], step)]
+            list(pool.map(lambda pr: oracle.gemm_rows(A, B, pr[0], pr[1]), parts))
+            return 2.0 * a.shape[0] * b.shape[0] * a.shape[1]
+
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=max(1, self.threads // 8)) as outer:
+            flops = sum(outer.map(one, self.jobs))
+        dt = time.perf_counter() - t0
+        pool.shutdown()
+        return flops, dt
 
 
 def cpu_cores():
@@ -504,12 +516,13 @@ def run_reference(args, dist):
     import oracle
     oracle.build()
     threads = cpu_cores()
-    rows = 16
+    rows = 128
+    sample_run = OracleLayerSample(rows, threads)
     for _ in range(args.warmup):
-        oracle_layer_sample(rows, threads)
+        sample_run.run()
     flops = secs = 0.0
     for _ in range(args.steps):
-        f, s = oracle_layer_sample(rows, threads)
+        f, s = sample_run.run()
         flops += f
         secs += s
     tflops = flops / secs / 1e12
@@ -533,8 +546,9 @@ def layer_config():
     import workloads
     return {
         "workload": ("transformer layer, 12 FP8 GEMMs (fprop/dgrad/wgrad x qkv/attn_out/mlp_up/"
-                     "mlp_down), 1x128 tiles on activations and gradients, 128x128 blocks on "
-                     "weights, E4M3 forward / E5M2 gradients, autocast (quantize included)"),
+                     "mlp_down), per-tensor current scaling (amax -> scale -> cast of x, w and "
+                     "grad_out each step), E4M3 forward / E5M2 gradients, autocast (quantize "
+                     "included)"),
         "M": workloads.TOKENS, "hidden": workloads.HIDDEN, "ffn": workloads.FFN,
         "inputs": "bf16 x~N(0,1), w~N(0,0.02), grad_out~N(0,1e-3) + 40.0 spikes per 1e6",
         "out_dtype": "bf16",
@@ -580,37 +594,28 @@ def main():
     K, W = args.steps, args.warmup
     flops = state.flops
 
-    # ---- headline: block-scaled layer, autocast
-    with ClockSampler(uuid) as clk:
-        ms_auto = time_steps(torch, dist, stream, run.block_autocast, K, W, record=run)
-    gemm_ev = run.gemm_events
-    run.gemm_events = None
-    gemm_ms = sum(a.elapsed_time(b) for a, b, _ in gemm_ev)
-    gemm_fl = sum(f for _, _, f in gemm_ev)
-    n_gemm = len(gemm_ev)
-    quant_ms_per_step = ms_auto - gemm_ms / K
+    def gemm_summary(events):
+        ms = sum(a.elapsed_time(b) for a, b, _ in events)
+        fl = sum(f for _, _, f in events)
+        return ms, fl, len(events)
 
-    ms_pre = time_steps(torch, dist, stream, run.block_prequant, K, W, record=run)
-    pre_ev = run.gemm_events
+    # ---- headline: the layer with per-tensor current scaling, autocast
+    with ClockSampler(uuid) as clk:
+        ms_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(False), K, W,
+                             record=run)
+    t_gemm_ms, t_gemm_fl, t_gemm_n = gemm_summary(run.gemm_events)
     run.gemm_events = None
-    ms_t_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(False), K, W)
-    fq.fp8_quantize_tile1x128  # noqa: B018 (keep name visible in profiles)
-    run.quantize_block()       # operands for the per-tensor prequant GEMMs are refreshed below
-    for L in state.linears:
-        fq.fp8_amax(L["x"], out=L["ax"], stream=stream)
-        fq.fp8_amax(L["w"], out=L["aw"], stream=stream)
-        fq.fp8_amax(L["g"], out=L["ag"], stream=stream)
-        fq.fp8_quantize_tensor(L["x"], fq.E4M3, L["ax"], want_qt=True, q=L["qx"], q_t=L["qxt"],
-                               scale=L["tx"], stream=stream)
-        fq.fp8_quantize_tensor(L["w"], fq.E4M3, L["aw"], want_qt=True, q=L["qw"], q_t=L["qwt"],
-                               scale=L["tw"], stream=stream)
-        fq.fp8_quantize_tensor(L["g"], fq.E5M2, L["ag"], want_qt=True, q=L["qg"], q_t=L["qgt"],
-                               scale=L["tg"], stream=stream)
-    ms_t_pre = time_steps(torch, dist, stream, run.tensor_prequant, K, W)
+    ms_pre = time_steps(torch, dist, stream, run.tensor_prequant, K, W)
     ms_d_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(True), K, W)
 
-    # ---- end to end through host buffers
-    ms_e2e = time_steps(torch, dist, stream, run.e2e_block, max(2, K // 2), 1)
+    # ---- the same layer with 1x128 / 128x128 scaling
+    ms_b_auto = time_steps(torch, dist, stream, run.block_autocast, K, W, record=run)
+    b_gemm_ms, b_gemm_fl, b_gemm_n = gemm_summary(run.gemm_events)
+    run.gemm_events = None
+    ms_b_pre = time_steps(torch, dist, stream, run.block_prequant, K, W)
+
+    # ---- end to end through host buffers (headline recipe)
+    ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), 1)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
     xq, _ = workloads.quantize_activation()
@@ -653,8 +658,8 @@ def main():
         import oracle
         oracle.build()
         threads = cpu_cores()
-        rows = 32
-        f, s = oracle_layer_sample(rows, threads)
+        rows = 512
+        f, s = OracleLayerSample(rows, threads).run()
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": (f"{rows} output rows x 128 columns of each of the 12 layer GEMMs "
                           f"(oracle quantises those A rows and one 128-row B block, then "
@@ -664,14 +669,16 @@ def main():
     fp8_peak_sust = FP8_PER_BF16 * float(peaks.get("bf16_tflops_sustained",
                                                    FALLBACK_PEAKS["bf16_tflops_sustained"]))
     fp8_peak_burst = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    gemm_tflops = gemm_fl / (gemm_ms * 1e-3) / 1e12
-    pre_tflops = flops / (ms_pre * 1e-3) / 1e12
+    t_gemm_tflops = t_gemm_fl / (t_gemm_ms * 1e-3) / 1e12
+    b_gemm_tflops = b_gemm_fl / (b_gemm_ms * 1e-3) / 1e12
     tile_gbps = gbps(tile_bytes, ms_tile)
+    tf = lambda ms: flops / (ms * 1e-3) / 1e12
+    peak_src = (f"{peak_src}: bf16_tflops_sustained x {FP8_PER_BF16} (dense FP8/BF16 nominal "
+                "ratio)")
 
-    launches_per_step = Runner.block_autocast.launches
     line = {
         "metric": METRIC,
-        "value": flops / (ms_auto * 1e-3) / 1e12,
+        "value": tf(ms_auto),
         "unit": "TFLOP/s",
         "n_gpus": dist.world,
         "steps": K,
@@ -683,16 +690,26 @@ def main():
         "dtype": "fp8->f32",
         "data": "synthetic",
         "config": layer_config(),
-        "prequant": {"value": pre_tflops, "unit": "TFLOP/s", "ms_per_step": ms_pre},
-        "quantize_ms_per_step": quant_ms_per_step,
-        "per_tensor_current": {
-            "autocast": {"value": flops / (ms_t_auto * 1e-3) / 1e12, "ms_per_step": ms_t_auto},
-            "prequant": {"value": flops / (ms_t_pre * 1e-3) / 1e12, "ms_per_step": ms_t_pre},
-            "unit": "TFLOP/s"},
-        "per_tensor_delayed_grad": {
-            "autocast": {"value": flops / (ms_d_auto * 1e-3) / 1e12, "ms_per_step": ms_d_auto},
+        "prequant": {"value": tf(ms_pre), "unit": "TFLOP/s", "ms_per_step": ms_pre},
+        "quantize_ms_per_step": ms_auto - t_gemm_ms / K,
+        "delayed_grad": {
+            "autocast": {"value": tf(ms_d_auto), "ms_per_step": ms_d_auto}, "unit": "TFLOP/s",
+            "note": "grad_out cast with its amax history (delayed scaling), x and w current"},
+        "block_scaled": {
+            "workload": ("the same 12 GEMMs with 1x128 tiles on activations and gradients and "
+                         "128x128 blocks on weights"),
+            "autocast": {"value": tf(ms_b_auto), "ms_per_step": ms_b_auto},
+            "prequant": {"value": tf(ms_b_pre), "ms_per_step": ms_b_pre},
             "unit": "TFLOP/s",
-            "note": "grad_out cast with the amax history (delayed), x and w current"},
+            "roofline": {"bound": "tensor", "achieved": b_gemm_tflops, "peak": fp8_peak_sust,
+                         "unit": "TFLOP/s", "frac": b_gemm_tflops / fp8_peak_sust,
+                         "traffic": None, "kernel": "gemm_blockscaled_kernel",
+                         "launches": b_gemm_n}},
+        "context_pages_B300_ms_per_layer": {
+            "fp8_current_autocast": 9.15, "fp8_current_prequant": 6.81,
+            "fp8_delayed_autocast": 7.80, "mxfp8_autocast": 8.98,
+            "note": ("the blog repost's CodonFM-5B layer on B300 with Transformer Engine; "
+                     "context, not the target")},
         "quantize": {
             "workload": "8192x4096 bf16 activation (1% rows x 1e4), E4M3, L2 flushed per call",
             "tile1x128": {"GB/s": tile_gbps, "us": ms_tile * 1e3,
@@ -704,22 +721,20 @@ def main():
                                "frac": gbps(3 * n, ms_tensor) / hbm_peak},
             "unit": "GB/s", "peak": hbm_peak,
         },
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak_sust,
-                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_sust, "traffic": None,
-                     "kernel": "gemm_blockscaled_kernel (12 GEMMs of the autocast step)",
-                     "launches": n_gemm,
-                     "peak_source": (f"{peak_src}: bf16_tflops_sustained x {FP8_PER_BF16} "
-                                     "(dense FP8/BF16 nominal ratio)"),
-                     "frac_of_burst": gemm_tflops / fp8_peak_burst},
+        "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,
+                     "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_sust, "traffic": None,
+                     "kernel": "gemm_tensor_kernel (12 GEMMs of the autocast step)",
+                     "launches": t_gemm_n, "peak_source": peak_src,
+                     "frac_of_burst": t_gemm_tflops / fp8_peak_burst},
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,
                               "unit": "GB/s", "frac": tile_gbps / hbm_peak, "traffic": None,
                               "kernel": "quant2d_kernel (1x128 row tiles)",
-                              "peak_source": f"{peak_src}: hbm_gbs"},
+                              "peak_source": "measured: hbm_gbs"},
         "cpu_baseline": cpu,
-        "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": tf(ms_e2e), "unit": "TFLOP/s",
                 "ms_per_step": ms_e2e, "h2d_bytes_per_step": state.h2d_bytes,
                 "d2h_bytes_per_step": state.d2h_bytes},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": Runner.tensor_autocast.launches * K,
         "clocks": clk.summary(),
     }
     if fq.device_status() != 0:

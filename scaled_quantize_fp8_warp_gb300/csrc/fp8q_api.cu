@@ -191,6 +191,7 @@ int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows, int64_t cols,
   p.format = format;
   p.saturate = saturate;
   p.mode = kModeTensorCurrent;
+  p.err = device_error_word();
   p.amax_in = amax;
   p.scale_out = scale_out;
   p.q = q;
@@ -219,6 +220,7 @@ int fp8_quantize_delayed(const void *x, int in_dtype, int64_t rows, int64_t cols
   p.format = format;
   p.saturate = saturate;
   p.mode = kModeTensorDelayed;
+  p.err = device_error_word();
   p.hist = hist;
   p.scale_out = scale_out;
   p.q = q;
@@ -265,6 +267,7 @@ int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows, int64_t co
   p.format = format;
   p.saturate = saturate;
   p.mode = kModeTile;
+  p.err = device_error_word();
   p.q = want_row ? q : nullptr;
   p.q_scales = want_row ? q_scales : nullptr;
   p.q_t = want_col ? q_t : nullptr;
@@ -294,6 +297,7 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t
   p.format = format;
   p.saturate = saturate;
   p.mode = kModeBlock;
+  p.err = device_error_word();
   p.q = q;
   p.q_t = q_t;
   p.q_scales = block_scales;

@@ -41,7 +41,13 @@ constexpr int kBM = 128;
 constexpr int kBK = 128;            // bytes = FP8 elements per K block
 constexpr int kUmmaK = 32;          // K per tcgen05.mma for 8-bit inputs
 constexpr int kGroupM = 16;         // M-tiles per raster group
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Tile width and promotion warpgroups of the tile/block-scaled kernel.
+#ifndef FP8Q_BLOCK_BN
+#define FP8Q_BLOCK_BN 256
+#define FP8Q_BLOCK_WG 2
+#endif
+constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
+constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 
 struct GemmArgs {
   int64_t M, N, K;
@@ -65,35 +71,6 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   const int local = tile - g * per_group;
   mt = first_m + local % gsize;
   nt = local / gsize;
-}
-
-// Bounded wait.  Returns false when the CTA is aborting (this call timed out
-// or another role already did).
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                             volatile int *abort_flag, unsigned int *err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
-        atomicOr(err, 1u);
-        return false;
-      }
-    }
-  }
-}
-
-// Warp-uniform variant: lane 0 waits, the verdict is broadcast.
-__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
-                                                  volatile int *abort_flag, unsigned int *err) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, err) ? 1 : 0;
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  return ok != 0;
 }
 
 template <int BN, int STAGES>
@@ -313,35 +290,49 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ------------------------------------------------------------------------
-// Tile/block scaled GEMM: 12 warps -- warpgroup 0 holds the producer (warp 0)
-// and the MMA issuer (warp 1); warpgroups 1 and 2 are promotion warps, each
-// warpgroup owning 128 of the 256 tile columns.  A carries 1x128
-// tile scales; B carries 128x128 block scales (B_TILE = false) or 1x128 tile
-// scales (B_TILE = true).
+// Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0) and the MMA
+// issuer (warp 1); NWG promotion warpgroups follow, warpgroup g owning tile
+// columns [g C, g C + C) with C = BN / NWG.  A carries 1x128 tile scales; B
+// carries 128x128 block scales (B_TILE = false) or 1x128 tile scales
+// (B_TILE = true).  Each 128-wide K block is accumulated into one of two
+// TMEM buffers of BN columns; the promotion warps load their C columns of it
+// (64 per round trip), hand the buffer back, and add it into fp32 registers
+// with the block's scale product.
+//
+// Register split (setmaxnreg inside each role's branch): the launch of
+// 128 (1 + NWG) threads gets kLaunchRegs per thread; warpgroup 0 drops to
+// kLowRegs and the promotion warpgroups rise to kHighRegs, with
+// 128 kLowRegs + 128 NWG kHighRegs <= 128 (1 + NWG) kLaunchRegs.  The host
+// checks the compiled launch count before the first launch.
 // ------------------------------------------------------------------------
-constexpr int kBSBN = 256;
-constexpr int kBSStages = 4;
-constexpr int kBSThreads = 384;
-// Register split (setmaxnreg, inside each role's branch): the 384-thread launch
-// gets 168 registers per thread (65536 / 384 rounded down to 8); warpgroup 0
-// (producer, MMA, two idle warps) drops to 40, the two promotion warpgroups
-// rise to 232: 128 * 40 + 256 * 232 = 64512 = 384 * 168.  The host checks
-// the compiled launch count before the first launch.
-constexpr int kBSLaunchRegs = 168;
-constexpr int kBSLowRegs = 40;
-constexpr int kBSHighRegs = 232;
-static_assert(128 * kBSLowRegs + 256 * kBSHighRegs <= kBSThreads * kBSLaunchRegs,
-              "register split exceeds the launch allocation");
+template <int BN, int NWG>
+struct BSConfig {
+  static constexpr int kThreads = 128 * (1 + NWG);
+  static constexpr int kCols = BN / NWG;                 // columns per promotion warpgroup
+  static constexpr int kStages = BN <= 192 ? 5 : 4;
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr int kLowRegs = NWG == 2 ? 40 : 56;
+  static constexpr int kHighRegs = ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8 > 232
+                                       ? 232
+                                       : ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8;
+  static constexpr uint32_t kTmemCols = 512;              // two BN-column buffers fit
+  static_assert(BN % NWG == 0 && (kCols == 64 || kCols == 128), "64 or 128 columns per WG");
+  static_assert(2 * BN <= 512, "two partial-sum buffers must fit in TMEM");
+  static_assert(128 * kLowRegs + 128 * NWG * kHighRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+};
 
-template <bool B_TILE, bool OUT_BF16>
-__global__ void __launch_bounds__(kBSThreads, 1)
+template <int BN, int NWG, bool B_TILE, bool OUT_BF16>
+__global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap ta,
                             const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
-  constexpr int BN = kBSBN, STAGES = kBSStages;
+  using Cfg = BSConfig<BN, NWG>;
+  constexpr int STAGES = Cfg::kStages;
+  constexpr int C = Cfg::kCols;
+  constexpr int NPW = 4 * NWG;   // promotion warps
   using L = Layout<BN, STAGES>;
-  constexpr uint32_t kTmemCols = 512;  // two 256-column partial-sum buffers
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(16) float sh_bscale[8][128];  // per promotion warp: B tile scales
+  __shared__ __align__(16) float sh_bscale[NPW][C];  // per promotion warp: B tile scales
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -361,7 +352,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(pf0 + 8 * b, 1);
-      mbar_init(pe0 + 8 * b, 8);
+      mbar_init(pe0 + 8 * b, NPW);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -371,7 +362,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
     prefetch_tmap(&tb);
   }
   if (warp == 1) {
-    tmem_alloc(slot, kTmemCols);
+    tmem_alloc(slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -382,44 +373,40 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   const int nkb = p.num_k_blocks;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kBSLowRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kLowRegs));
     if (warp == 0) {
       if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
       __syncwarp();
     } else if (warp == 1) {
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-          if (!wait_bounded(pe0 + 8 * pb, pph ^ 1u, abort_flag, p.err) ||
-              !wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
-            ok = false;
-            break;
+      if (lane == 0) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+            if (!wait_bounded(pe0 + 8 * pb, pph ^ 1u, abort_flag, p.err) ||
+                !wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
+            mma_commit(empty0 + 8 * s);
+            mma_commit(pf0 + 8 * pb);
           }
-          tc_fence_after();
-          issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
-          mma_commit(empty0 + 8 * s);
-          mma_commit(pf0 + 8 * pb);
         }
+        drain_mma(drain, abort_flag);
       }
-      drain_mma(drain, abort_flag);
-    }
-    __syncwarp();
+      __syncwarp();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kBSHighRegs));
-    // Promotion warps 4..11: warpgroup wg owns tile columns [128 wg, 128 wg + 128);
-    // TMEM lane quarter = warp % 4.  Scales for K block kb + 1 are fetched
-    // into registers while block kb is promoted; B tile scales go through a
-    // per-warp shared buffer guarded by __syncwarp only (no cross-warp
-    // barrier, so an aborting warp can never strand the others).
-    const int pw = warp - 4;           // 0..7
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kHighRegs));
+    const int pw = warp - 4;              // promotion warp 0 .. NPW-1
     const int wg = pw >> 2;
-    const int quarter = warp & 3;
+    const int quarter = warp & 3;         // TMEM lane quarter of this warp
     float *my_bs = sh_bscale[pw];
+    constexpr int kPerLane = C / 32;      // B tile scales each lane stages (2 or 4)
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -427,44 +414,48 @@ __global__ void __launch_bounds__(kBSThreads, 1)
       tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
       const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
       const bool m_ok = m < p.M;
-      const int64_t ncol0 = (int64_t)nt * BN + wg * 128;  // first column of this warpgroup
-      const int64_t nblk = ncol0 / 128;
-      const bool nblk_ok = ncol0 < p.N;
-      const int64_t nl = ncol0 + lane * 4;                 // this lane's 4 B-scale columns
+      const int64_t ncol0 = (int64_t)nt * BN + wg * C;   // first column of this warpgroup
+      const int64_t nl = ncol0 + lane * kPerLane;         // this lane's B-scale columns
       auto load_sa = [&](int kb) -> float {
         return m_ok ? p.scale_a[kb * p.a_stride_k + m * p.a_stride_row] : 0.0f;
       };
+      // Block scales: a warpgroup's C columns may straddle two 128-column
+      // blocks when C = 64 only if ncol0 % 128 == 64; both halves of a
+      // 64-column group lie in one block, so one scale serves the group.
       auto load_sb = [&](int kb) -> float {
-        return nblk_ok ? p.scale_b[nblk * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
+        return ncol0 < p.N ? p.scale_b[(ncol0 / 128) * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
       };
-      auto load_sb4 = [&](int kb) -> float4 {
-        float4 f;
-        const float *base = p.scale_b + kb * p.b_stride_k;
-        f.x = (nl + 0 < p.N) ? base[(nl + 0) * p.b_stride_row] : 0.0f;
-        f.y = (nl + 1 < p.N) ? base[(nl + 1) * p.b_stride_row] : 0.0f;
-        f.z = (nl + 2 < p.N) ? base[(nl + 2) * p.b_stride_row] : 0.0f;
-        f.w = (nl + 3 < p.N) ? base[(nl + 3) * p.b_stride_row] : 0.0f;
-        return f;
-      };
-      float acc[128];
+      float acc[C];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < C; ++j) acc[j] = 0.0f;
       float sa_next = load_sa(0);
       float sb_next = B_TILE ? 0.0f : load_sb(0);
-      float4 sb4_next = B_TILE ? load_sb4(0) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float sbt_next[kPerLane];
+      if (B_TILE) {
+#pragma unroll
+        for (int u = 0; u < kPerLane; ++u)
+          sbt_next[u] = (nl + u < p.N) ? p.scale_b[(nl + u) * p.b_stride_row] : 0.0f;
+      }
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const float sa = sa_next;
         const float sb = sb_next;
-        const float4 sb4 = sb4_next;
-        if (kb + 1 < nkb) {
-          sa_next = load_sa(kb + 1);
-          if (B_TILE) sb4_next = load_sb4(kb + 1);
-          else sb_next = load_sb(kb + 1);
-        }
         if (B_TILE) {
           __syncwarp();
-          *reinterpret_cast<float4 *>(&my_bs[lane * 4]) = sb4;
+#pragma unroll
+          for (int u = 0; u < kPerLane; ++u) my_bs[lane * kPerLane + u] = sbt_next[u];
           __syncwarp();
+        }
+        if (kb + 1 < nkb) {
+          sa_next = load_sa(kb + 1);
+          if (B_TILE) {
+#pragma unroll
+            for (int u = 0; u < kPerLane; ++u)
+              sbt_next[u] = (nl + u < p.N)
+                                ? p.scale_b[(kb + 1) * p.b_stride_k + (nl + u) * p.b_stride_row]
+                                : 0.0f;
+          } else {
+            sb_next = load_sb(kb + 1);
+          }
         }
         const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
         if (!wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
@@ -474,15 +465,15 @@ __global__ void __launch_bounds__(kBSThreads, 1)
         tc_fence_after();
         const float sab = __fmul_rn(sa, sb);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < C / 64; ++h) {
           // 64 columns per round trip: two 32-column TMEM loads, one wait
           uint32_t r0[32], r1[32];
-          const uint32_t col = pb * BN + wg * 128 + h * 64;
+          const uint32_t col = pb * BN + wg * C + h * 64;
           const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
           tmem_ld_32x32b_x32(tmem_base + lane_base + col, r0);
           tmem_ld_32x32b_x32(tmem_base + lane_base + col + 32, r1);
           tmem_ld_wait();
-          if (h == 1) {
+          if (h == C / 64 - 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pe0 + 8 * pb);
@@ -508,7 +499,7 @@ __global__ void __launch_bounds__(kBSThreads, 1)
       if (!ok) break;
       if (m_ok) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < C / 32; ++c) {
           const int64_t n0 = ncol0 + c * 32;
           if (n0 < p.N) {
             float v[32];
@@ -524,39 +515,17 @@ __global__ void __launch_bounds__(kBSThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
 }
 
 // ------------------------------------------------------------------ host
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
 
 // Row-major [rows, K] byte matrix, box = box_k x box_rows, 128-byte swizzle,
 // out-of-bounds elements read as zero.
 bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K, uint32_t box_k,
                uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t gdim[2] = {K, rows};
-  cuuint64_t gstride[1] = {K};
-  cuuint32_t box[2] = {box_k, box_rows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), gdim, gstride,
-                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, box_k, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <typename KernelT>
@@ -578,26 +547,56 @@ int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, 
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-template <bool B_TILE, bool OUT_BF16>
+template <int BN, int NWG, bool B_TILE, bool OUT_BF16>
 int run_blockscaled(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                     cudaStream_t stream) {
-  using L = Layout<kBSBN, kBSStages>;
-  auto kernel = gemm_blockscaled_kernel<B_TILE, OUT_BF16>;
+  using Cfg = BSConfig<BN, NWG>;
+  using L = Layout<BN, Cfg::kStages>;
+  auto kernel = gemm_blockscaled_kernel<BN, NWG, B_TILE, OUT_BF16>;
   static bool attr_done = false;
   if (!attr_done) {
     // The setmaxnreg split is only safe if the kernel launches with at least
-    // kBSLaunchRegs registers per thread; refuse to launch otherwise.
+    // kLaunchRegs registers per thread; refuse to launch otherwise.
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (fa.numRegs < kBSLaunchRegs) return FP8Q_ERR_CUDA;
+    if (fa.numRegs < Cfg::kLaunchRegs) return FP8Q_ERR_CUDA;
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
     attr_done = true;
   }
-  kernel<<<grid, kBSThreads, L::kSmemBytes, stream>>>(ta, tb, a);
+  kernel<<<grid, Cfg::kThreads, L::kSmemBytes, stream>>>(ta, tb, a);
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
 }  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, uint64_t inner,
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t gdim[2] = {inner, outer};
+  cuuint64_t gstride[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = fn(m, dtype, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int out_dtype,
                 int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
@@ -614,7 +613,7 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
         (B.scaling != FP8Q_SCALE_TILE_1x128 && B.scaling != FP8Q_SCALE_BLOCK_128x128))
       return FP8Q_ERR_NOT_IMPLEMENTED;
   }
-  int BN = 256;
+  int BN = kBlockScaledBN;
   if (tensor) BN = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, kBK, kBM) ||
@@ -654,11 +653,12 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
                 : run_tensor<256, 4, false>(ta, tb, a, grid, stream);
   }
   const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
+  constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;
   if (b_tile)
-    return bf16 ? run_blockscaled<true, true>(ta, tb, a, grid, stream)
-                : run_blockscaled<true, false>(ta, tb, a, grid, stream);
-  return bf16 ? run_blockscaled<false, true>(ta, tb, a, grid, stream)
-              : run_blockscaled<false, false>(ta, tb, a, grid, stream);
+    return bf16 ? run_blockscaled<BBN, BWG, true, true>(ta, tb, a, grid, stream)
+                : run_blockscaled<BBN, BWG, true, false>(ta, tb, a, grid, stream);
+  return bf16 ? run_blockscaled<BBN, BWG, false, true>(ta, tb, a, grid, stream)
+              : run_blockscaled<BBN, BWG, false, false>(ta, tb, a, grid, stream);
 }
 
 }  // namespace fp8q

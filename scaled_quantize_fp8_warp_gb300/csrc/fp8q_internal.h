@@ -1,6 +1,7 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -16,6 +17,13 @@ unsigned int *device_error_word();
 
 // SM count of the current device (cached).
 int sm_count();
+
+// 2D tiled tensor map over a row-major matrix (outer rows of `inner`
+// elements, rows row_stride_bytes apart); out-of-bounds elements read as
+// zero.  False if the driver entry point is missing or rejects the shape.
+bool make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, uint64_t inner,
+                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                  uint32_t box_outer, CUtensorMapSwizzle swizzle);
 
 enum QuantMode : int {
   kModeTensorCurrent = 0,  // s from a device amax
@@ -38,6 +46,7 @@ struct QuantParams {
   uint8_t *q_t;                // [cols, rows] or null
   float *q_scales;             // tile: [ceil(cols/128), rows]; block: [nrb, ncb]
   float *qt_scales;            // tile: [ceil(rows/128), cols]
+  unsigned int *err;           // device error word (bounded waits)
 };
 
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,

@@ -172,5 +172,38 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t afmt, uint32_t bfmt
   return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// Wall-clock limit of every barrier wait in the library's kernels.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Bounded mbarrier wait.  Returns false when the CTA is aborting: this call
+// ran past kWaitLimitNs (it then raises the CTA's abort flag and records
+// error bit 1 in the device error word) or another thread already aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int *abort_flag, unsigned int *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+// Warp-uniform variant: lane 0 waits, the verdict is broadcast.
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort_flag, unsigned int *err) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bounded(bar, parity, abort_flag, err) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  return ok != 0;
+}
+
 }  // namespace ptx
 }  // namespace fp8q

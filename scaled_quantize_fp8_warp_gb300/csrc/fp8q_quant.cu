@@ -23,10 +23,13 @@
 // is a shuffle butterfly inside each half-warp; column amax for 128x1 tiles
 // goes through shared memory; the transposed FP8 copy is an in-register 8x8
 // byte transpose (uniform scales) or a second cast (column-tile scales).
+#include <cuda.h>
 #include <cuda_fp8.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "fp8q_internal.h"
+#include "fp8q_ptx.cuh"
 
 namespace fp8q {
 namespace {
@@ -73,6 +76,20 @@ __device__ __forceinline__ uint32_t cvt2(float lo, float hi) {
                                              FmtTraits<FMT>::kInterp);
 }
 
+// Two fp32 values (x -> low byte, y -> high byte) -> two FP8 bytes.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_pair(float2 v) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, FmtTraits<FMT>::kInterp);
+}
+
+// Correctly rounded x / s for a pair, packed two-wide (see the file comment;
+// nsn = (-s, -s), r2 = (r, r)).  Signs of zero results are fixed by the caller.
+__device__ __forceinline__ float2 div2_fast(float2 x, float2 nsn, float2 r2) {
+  const float2 q0 = __fmul2_rn(x, r2);
+  const float2 e = __ffma2_rn(q0, nsn, x);
+  return __ffma2_rn(e, r2, q0);
+}
+
 // Full-rule encode for the slow path: NaN -> 0x7F | sign; without saturation
 // an overflowing quotient becomes NaN (E4M3) or Inf (E5M2).
 template <int FMT>
@@ -92,11 +109,16 @@ __device__ __forceinline__ uint32_t encode_slow(float v, int saturate) {
 
 template <int FMT>
 __device__ __forceinline__ uint2 cast8_fast(const float (&v)[8], float s, float r) {
-  uint32_t p0 = cvt2<FMT>(div_fast(v[0], s, r), div_fast(v[1], s, r));
-  uint32_t p1 = cvt2<FMT>(div_fast(v[2], s, r), div_fast(v[3], s, r));
-  uint32_t p2 = cvt2<FMT>(div_fast(v[4], s, r), div_fast(v[5], s, r));
-  uint32_t p3 = cvt2<FMT>(div_fast(v[6], s, r), div_fast(v[7], s, r));
-  return make_uint2(p0 | (p1 << 16), p2 | (p3 << 16));
+  const float2 nsn = make_float2(-s, -s), r2 = make_float2(r, r);
+  uint32_t p[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float2 q = div2_fast(make_float2(v[2 * k], v[2 * k + 1]), nsn, r2);
+    q.x = copysignf(q.x, v[2 * k]);       // a zero quotient keeps x's sign
+    q.y = copysignf(q.y, v[2 * k + 1]);
+    p[k] = cvt_pair<FMT>(q);
+  }
+  return make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
 }
 
 // Slow path per element: a NaN input keeps its sign (0x7F | sign); a NaN the
@@ -144,6 +166,9 @@ struct Row8<uint16_t> {
     w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + idx));
   }
   __device__ __forceinline__ void zero() { w = make_uint4(0u, 0u, 0u, 0u); }
+  __device__ __forceinline__ void load_smem(const uint8_t *row_base) {
+    w = *reinterpret_cast<const uint4 *>(row_base);
+  }
   __device__ __forceinline__ uint32_t word(int k) const {
     return k == 0 ? w.x : (k == 1 ? w.y : (k == 2 ? w.z : w.w));
   }
@@ -181,6 +206,11 @@ struct Row8<float> {
     b = __ldg(p + 1);
   }
   __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void load_smem(const uint8_t *row_base) {
+    const float4 *q = reinterpret_cast<const float4 *>(row_base);
+    a = q[0];
+    b = q[1];
+  }
   __device__ __forceinline__ float at(int j) const {
     switch (j) {
       case 0: return a.x; case 1: return a.y; case 2: return a.z; case 3: return a.w;
@@ -203,13 +233,44 @@ struct Row8<float> {
   }
 };
 
-template <int FMT, typename InT>
-__device__ __forceinline__ uint2 cast_row(const Row8<InT> &x, float s, float r, bool fast,
-                                          int saturate) {
+// Fast cast of one 8-element bf16 row chunk straight from its packed words:
+// pairs are widened, divided two-wide and converted two at a time; the FP8
+// sign bits are then OR-ed in from the bf16 sign bits (bit 7 of bytes 1 and
+// 3 of each word), which is exact for every finite x (a negative x always
+// has a negative code, -0 included) and fixes zero quotients.
+template <int FMT>
+__device__ __forceinline__ uint2 cast_row_fast(const Row8<uint16_t> &x, float s, float r) {
+  const float2 nsn = make_float2(-s, -s), r2 = make_float2(r, r);
+  uint32_t p[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = x.word(k);
+    p[k] = cvt_pair<FMT>(div2_fast(
+        make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), nsn, r2));
+  }
+  const uint32_t lo = __byte_perm(p[0], p[1], 0x5410) |
+                      (__byte_perm(x.w.x, x.w.y, 0x7531) & 0x80808080u);
+  const uint32_t hi = __byte_perm(p[2], p[3], 0x5410) |
+                      (__byte_perm(x.w.z, x.w.w, 0x7531) & 0x80808080u);
+  return make_uint2(lo, hi);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 cast_row_fast(const Row8<float> &x, float s, float r) {
   float v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = x.at(j);
-  return cast8<FMT>(v, s, r, fast, saturate);
+  return cast8_fast<FMT>(v, s, r);
+}
+
+template <int FMT, typename InT>
+__device__ __forceinline__ uint2 cast_row(const Row8<InT> &x, float s, float r, bool fast,
+                                          int saturate) {
+  if (fast) return cast_row_fast<FMT>(x, s, r);
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = x.at(j);
+  return cast8_slow<FMT>(v, s, saturate);
 }
 
 // 4x4 byte transpose: a..d are rows (byte k = column k); o0..o3 are columns.
@@ -248,17 +309,33 @@ enum KernelMode : int {
   kKBlock = 5       // 128x128 blocks -> q and/or q_t, block scales
 };
 
+// Input tiles (128 x 128 elements) reach shared memory by TMA through a ring
+// of kStages buffers; thread 0 refills a buffer as soon as every thread has
+// copied its part of the previous tile out of it, so up to kStages tiles per
+// CTA are in flight while earlier ones are converted and stored.
+template <typename InT>
+struct QuantRing {
+  static constexpr int kTileBytes = 128 * 128 * (int)sizeof(InT);
+  static constexpr int kStages = sizeof(InT) == 2 ? 3 : 2;
+  static constexpr int kSmemBytes = kStages * kTileBytes + 1024;  // + alignment slack
+};
+
 template <typename InT, int FMT, int KM>
-__global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantParams p) {
+__global__ void __launch_bounds__(kQuantThreads, 2)
+    quant2d_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr bool kRowTiles = (KM == kKTileRow || KM == kKTileBoth);
   constexpr bool kColTiles = (KM == kKTileCol || KM == kKTileBoth);
   constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock);
+  using Ring = QuantRing<InT>;
   const float fm = FmtTraits<FMT>::kMax;
 
+  extern __shared__ uint8_t dyn_smem[];
   __shared__ float sh_row_s[128], sh_row_r[128];
   __shared__ float sh_col_s[128], sh_col_r[128];
   __shared__ uint32_t sh_colmax[8][128];
   __shared__ uint32_t sh_red[8];
+  __shared__ __align__(8) uint64_t sh_full[Ring::kStages];
+  __shared__ int sh_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = warp * 2 + (lane >> 4);
@@ -267,6 +344,40 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantPa
   const int64_t tiles_c = (cols + 127) / 128, tiles_r = (rows + 127) / 128;
   const int64_t ntiles = tiles_r * tiles_c;
   const int saturate = p.saturate;
+  const uint32_t raw = ptx::smem_u32(dyn_smem);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint8_t *ring_ptr = dyn_smem + (ring - raw);
+  volatile int *abort_flag = &sh_abort;
+
+  // Tiles of this CTA: blockIdx.x + i * gridDim.x.  Per-tensor current
+  // scaling runs right after the amax pass over the same data, so it walks
+  // the tiles backwards and meets the most recently read (still L2-resident)
+  // part of x first.
+  const int64_t my_tiles =
+      (blockIdx.x < ntiles) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto tile_of = [&](int64_t i) -> int64_t {
+    const int64_t t = blockIdx.x + i * gridDim.x;
+    return (KM == kKTensor) ? (ntiles - 1 - t) : t;
+  };
+  auto issue = [&](int64_t i) {
+    const int s = (int)(i % Ring::kStages);
+    const int64_t tt = tile_of(i);
+    const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
+    const uint32_t bar = ptx::smem_u32(&sh_full[s]);
+    ptx::mbar_arrive_expect_tx(bar, Ring::kTileBytes);
+    ptx::tma_load_2d(ring + s * Ring::kTileBytes, &tmx, (int32_t)(tc * 128), (int32_t)(tr * 128),
+                     bar);
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < Ring::kStages; ++s) ptx::mbar_init(ptx::smem_u32(&sh_full[s]), 1);
+    sh_abort = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+    if (my_tiles > 0) ptx::prefetch_tmap(&tmx);
+    for (int64_t i = 0; i < my_tiles && i < Ring::kStages; ++i) issue(i);
+  }
+  __syncthreads();
 
   float s_u = 0.0f, r_u = 0.0f;
   if (KM == kKTensor) {
@@ -280,12 +391,15 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantPa
     r_u = __fdiv_rn(1.0f, s_u);
   }
   uint32_t run_max = 0;  // delayed: running max |x| of this CTA
+  int64_t issued = my_tiles < Ring::kStages ? my_tiles : Ring::kStages;  // thread 0's count
 
-  for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    // Per-tensor current scaling runs right after the amax pass over the same
-    // data; walking the tiles backwards meets the most recently read (still
-    // L2-resident) part of x first.
-    const int64_t tt = (KM == kKTensor) ? (ntiles - 1 - t) : t;
+  // Every thread runs every iteration (and every __syncthreads) even after an
+  // abort; an aborted CTA only skips the work.
+  for (int64_t i = 0; i < my_tiles; ++i) {
+    const int s = (int)(i % Ring::kStages);
+    const uint32_t parity = (uint32_t)((i / Ring::kStages) & 1);
+    const bool ok = ptx::wait_bounded_warp(ptx::smem_u32(&sh_full[s]), parity, abort_flag, p.err);
+    const int64_t tt = tile_of(i);
     const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
     const int64_t r0 = tr * 128, c0 = tc * 128;
     const int64_t cbase = c0 + cg * 8;
@@ -293,11 +407,25 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantPa
     const bool col_ok = cbase < cols;
     const bool rchunk_ok = rbase < rows;
 
+    // Copy this thread's 8 x 8 block out of the staged tile (row-major,
+    // 128 elements per row; out-of-bounds rows and columns were zero-filled).
     Row8<InT> v[8];
+    const uint8_t *tile_ptr = ring_ptr + s * Ring::kTileBytes;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (col_ok && rbase + i < rows) v[i].load(p.x, (rbase + i) * cols + cbase);
-      else v[i].zero();
+    for (int r = 0; r < 8; ++r) {
+      if (ok) v[r].load_smem(tile_ptr + ((rg * 8 + r) * 128 + cg * 8) * (int)sizeof(InT));
+      else v[r].zero();
+    }
+    // One CTA-wide verdict (every thread takes the same branch below, so the
+    // __syncthreads sequence stays identical); this barrier also frees buffer s.
+    const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (tid == 0 && i + Ring::kStages < my_tiles && !*abort_flag) {
+      issue(i + Ring::kStages);
+      issued = i + Ring::kStages + 1;
+    }
+    if (!all_ok) {
+      __syncthreads();
+      continue;
     }
 
     uint32_t rowmax[8];
@@ -433,6 +561,17 @@ __global__ void __launch_bounds__(kQuantThreads, 2) quant2d_kernel(const QuantPa
     __syncthreads();  // shared scratch is reused by the next tile
   }
 
+  if (*abort_flag && tid == 0) {
+    // Let copies still in flight land before the CTA exits (bounded).
+    for (int64_t j = (issued > Ring::kStages ? issued - Ring::kStages : 0); j < issued; ++j) {
+      const uint32_t bar = ptx::smem_u32(&sh_full[j % Ring::kStages]);
+      const uint32_t par = (uint32_t)((j / Ring::kStages) & 1);
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar, par) && ptx::globaltimer_ns() - t0 < 200000000ull) {
+      }
+    }
+  }
+
   // ------------------------------------------ per-tensor scale bookkeeping
   if (KM == kKTensor) {
     if (blockIdx.x == 0 && tid == 0 && p.scale_out != nullptr) *p.scale_out = s_u;
@@ -523,18 +662,35 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
 
 template <typename InT, int FMT, int KM>
 cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
+  using Ring = QuantRing<InT>;
+  auto kernel = quant2d_kernel<InT, FMT, KM>;
   static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks_per_sm, quant2d_kernel<InT, FMT, KM>, kQuantThreads, 0);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Ring::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, kQuantThreads,
+                                                      Ring::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
   }
+  // The input as a 2D tensor: cols elements per row, rows rows; one box is a
+  // 128 x 128 tile, out-of-bounds parts zero-filled.  rows == 0 or cols == 0
+  // launches no tile and leaves the map unused.
+  CUtensorMap tmx;
+  memset(&tmx, 0, sizeof tmx);
   const int64_t ntiles = ((p.rows + 127) / 128) * ((p.cols + 127) / 128);
+  if (ntiles > 0 &&
+      !make_tmap_2d(&tmx, p.x,
+                    sizeof(InT) == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                    (uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)p.cols * sizeof(InT), 128, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   int64_t grid = (int64_t)sm_count() * blocks_per_sm;
   if (ntiles < grid) grid = ntiles;
   if (grid < 1) grid = 1;
-  quant2d_kernel<InT, FMT, KM><<<(unsigned)grid, kQuantThreads, 0, stream>>>(p);
+  kernel<<<(unsigned)grid, kQuantThreads, Ring::kSmemBytes, stream>>>(tmx, p);
   return cudaGetLastError();
 }
 

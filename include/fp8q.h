@@ -123,6 +123,14 @@ int fp8q_device_status(void);
 /* 1 if the current device is compute capability 10.3, else 0. */
 int fp8q_device_supported(void);
 
+/* Self-test of the failure path: launches one warp that waits, through the
+ * library's bounded barrier wait, on an mbarrier nothing arrives at.  After
+ * the wait limit (about two seconds) the kernel records a timeout and
+ * returns; fp8q_device_status() then reports FP8Q_ERR_TIMEOUT once and the
+ * context stays usable.  Asynchronous on `stream`.
+ * Errors: ARCH, CUDA. */
+int fp8q_selftest_barrier_timeout(cudaStream_t stream);
+
 /* --------------------------------------------------------------- step a1 */
 
 /* amax = max |x| over n elements ([fp8_parity] scaled_roundtrip:

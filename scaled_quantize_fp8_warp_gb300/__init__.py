@@ -42,7 +42,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libfp8q.so")
 
 #: every symbol include/fp8q.h declares
 EXPORTS = (
-    "fp8q_status_string", "fp8q_device_status", "fp8q_device_supported", "fp8_amax",
+    "fp8q_status_string", "fp8q_device_status", "fp8q_device_supported",
+    "fp8q_selftest_barrier_timeout", "fp8_amax",
     "fp8_quantize_tensor", "fp8_quantize_delayed", "fp8q_history_init",
     "fp8_quantize_tile1x128", "fp8_quantize_block128x128", "fp8_gemm", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
@@ -84,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8q_status_string": (ctypes.c_char_p, [I32]),
             "fp8q_device_status": (I32, []),
             "fp8q_device_supported": (I32, []),
+            "fp8q_selftest_barrier_timeout": (I32, [P]),
             "fp8_amax": (I32, [P, I32, I64, P, P]),
             "fp8_quantize_tensor": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_delayed": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
@@ -389,6 +391,11 @@ def fp8_linear_autocast_noalloc(x, w, recipe=RECIPE_TENSOR_CURRENT, out_dtype=to
 def device_status() -> int:
     """Synchronise and read (and clear) the device error word."""
     return int(lib().fp8q_device_status())
+
+
+def selftest_barrier_timeout(stream=None) -> None:
+    """Launch the failure-path self-test (see include/fp8q.h)."""
+    _check(lib().fp8q_selftest_barrier_timeout(_stream(stream)), "fp8q_selftest_barrier_timeout")
 
 
 def device_supported() -> bool:

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fp8q_internal.h"
+#include "fp8q_ptx.cuh"
 
 namespace fp8q {
 namespace {
@@ -113,6 +114,22 @@ GemmOperandDev to_dev(const fp8q_operand *op) {
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// Self-test of the failure path: one warp waits, through the same bounded
+// wait the GEMM and quantize kernels use, on an mbarrier that nothing ever
+// arrives at.  After the wait's time limit it records the timeout in the
+// device error word and the kernel returns normally.
+__global__ void selftest_timeout_kernel(unsigned int *err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  (void)ptx::wait_bounded_warp(ptx::smem_u32(&bar), 0, &abort_flag, err);
+}
+
 }  // namespace
 
 unsigned int *device_error_word() {
@@ -162,6 +179,15 @@ int fp8q_device_status(void) {
     return FP8Q_ERR_TIMEOUT;
   }
   return FP8Q_OK;
+}
+
+int fp8q_selftest_barrier_timeout(cudaStream_t stream) {
+  int rc = check_device();
+  if (rc != FP8Q_OK) return rc;
+  unsigned int *err = device_error_word();
+  if (err == nullptr) return FP8Q_ERR_CUDA;
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(err);
+  return from_cuda(cudaGetLastError());
 }
 
 int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax, cudaStream_t stream) {

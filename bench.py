@@ -65,6 +65,8 @@ PROFILE_CASES = {
     "quant_tile_rows": "16384x8192 bf16, 1x128 row tiles, E4M3",
     "quant_block": "16384x8192 bf16, 128x128 blocks + transposed copy, E4M3",
     "amax": "16384x8192 bf16 amax",
+    "quant_activation": ("the bench's 8192x4096 activation, 1x128 row tiles, E4M3, L2 flushed "
+                         "before each of the three calls"),
 }
 
 
@@ -96,6 +98,13 @@ def run_profile_case(case: str):
         out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         for _ in range(3):
             fq.fp8_gemm(A, B, out=out)
+    elif case == "quant_activation":
+        x, _ = workloads.quantize_activation()
+        x = x.cuda()
+        flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            flush_buf.fill_(1.0)
+            fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True)
     else:
         x = workloads.normal((16384, 8192), 1.0, 902).cuda()
         for _ in range(3):
@@ -111,6 +120,25 @@ def run_profile_case(case: str):
     if fq.device_status() != 0:
         raise SystemExit("profile case: a kernel reported a barrier timeout")
     print(f"profile case {case} done: {PROFILE_CASES[case]}")
+
+
+def recorded_traffic(kernel_file: str, key: str):
+    """DRAM bytes per launch for a kernel, from profiles/roofline_traffic.json,
+    only if the kernel's source is unchanged since that capture (its sha256
+    is stored with the figure); otherwise None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
+    src = os.path.join(ROOT, "scaled_quantize_fp8_warp_gb300", "csrc", kernel_file)
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(key)
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_sha256") != digest:
+        return None
+    return rec.get("bytes_per_launch")
 
 
 def load_peaks():
@@ -389,6 +417,53 @@ class Runner:
 
     # end to end: host inputs in, host outputs out --------------------------
     def e2e_tensor(self):
+        """One step with the inputs copied in from pinned host memory and the
+        three outputs of every linear layer copied back, pipelined over three
+        streams: copy-in of layer i+1 and copy-out of layer i-1 overlap the
+        quantise + GEMMs of layer i (events order each layer's copies with
+        its compute; everything is ordered after the step's start on the
+        compute stream, and the compute stream waits for the last copy-out)."""
+        torch, fq, st = self.torch, self.fq, self.stream
+        if not hasattr(self, "_cin"):
+            self._cin, self._cout = torch.cuda.Stream(), torch.cuda.Stream()
+        start = torch.cuda.Event()
+        start.record(st)
+        self._cin.wait_event(start)
+        self._cout.wait_event(start)
+        arrived = []
+        for L in self.s.linears:
+            with torch.cuda.stream(self._cin):
+                L["x"].copy_(L["x_h"], non_blocking=True)
+                L["w"].copy_(L["w_h"], non_blocking=True)
+                L["g"].copy_(L["g_h"], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(self._cin)
+                arrived.append(ev)
+        for i, (L, o) in enumerate(zip(self.s.linears, self.tops)):
+            st.wait_event(arrived[i])
+            fq.fp8_amax(L["x"], out=L["ax"], stream=st)
+            fq.fp8_amax(L["w"], out=L["aw"], stream=st)
+            fq.fp8_amax(L["g"], out=L["ag"], stream=st)
+            fq.fp8_quantize_tensor(L["x"], fq.E4M3, L["ax"], want_q=True, want_qt=True, q=L["qx"],
+                                   q_t=L["qxt"], scale=L["tx"], stream=st)
+            fq.fp8_quantize_tensor(L["w"], fq.E4M3, L["aw"], want_q=True, want_qt=True, q=L["qw"],
+                                   q_t=L["qwt"], scale=L["tw"], stream=st)
+            fq.fp8_quantize_tensor(L["g"], fq.E5M2, L["ag"], want_q=True, want_qt=True,
+                                   q=L["qg"], q_t=L["qgt"], scale=L["tg"], stream=st)
+            for role in ("fprop", "dgrad", "wgrad"):
+                self._gemm(role, *o[role])
+            done = torch.cuda.Event()
+            done.record(st)
+            self._cout.wait_event(done)
+            with torch.cuda.stream(self._cout):
+                L["y_h"].copy_(L["y"], non_blocking=True)
+                L["dx_h"].copy_(L["dx"], non_blocking=True)
+                L["dw_h"].copy_(L["dw"], non_blocking=True)
+        fin = torch.cuda.Event()
+        fin.record(self._cout)
+        st.wait_event(fin)
+
+    def e2e_tensor_serial(self):
         st = self.stream
         with self.torch.cuda.stream(st):
             for L in self.s.linears:
@@ -635,6 +710,7 @@ def main():
         with torch.cuda.stream(stream):
             flush_buf.fill_(1.0)
             flush_sink.copy_(flush_buf.sum())
+            torch.cuda._sleep(400_000)   # ~0.2 ms more queue ahead of the start event
 
     qt = torch.empty((R, C), dtype=torch.uint8, device=xq.device)
     st = torch.empty(((C + 127) // 128, R), dtype=torch.float32, device=xq.device)
@@ -703,7 +779,8 @@ def main():
             "unit": "TFLOP/s",
             "roofline": {"bound": "tensor", "achieved": b_gemm_tflops, "peak": fp8_peak_sust,
                          "unit": "TFLOP/s", "frac": b_gemm_tflops / fp8_peak_sust,
-                         "traffic": None, "kernel": "gemm_blockscaled_kernel",
+                         "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_blockscaled_kernel"),
+                         "kernel": "gemm_blockscaled_kernel",
                          "launches": b_gemm_n}},
         "context_pages_B300_ms_per_layer": {
             "fp8_current_autocast": 9.15, "fp8_current_prequant": 6.81,
@@ -722,12 +799,14 @@ def main():
             "unit": "GB/s", "peak": hbm_peak,
         },
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,
-                     "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_sust, "traffic": None,
+                     "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_sust,
+                     "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_tensor_kernel"),
                      "kernel": "gemm_tensor_kernel (12 GEMMs of the autocast step)",
                      "launches": t_gemm_n, "peak_source": peak_src,
                      "frac_of_burst": t_gemm_tflops / fp8_peak_burst},
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,
-                              "unit": "GB/s", "frac": tile_gbps / hbm_peak, "traffic": None,
+                              "unit": "GB/s", "frac": tile_gbps / hbm_peak,
+                              "traffic": recorded_traffic("fp8q_quant.cu", "quant2d_tile_rows"),
                               "kernel": "quant2d_kernel (1x128 row tiles)",
                               "peak_source": "measured: hbm_gbs"},
         "cpu_baseline": cpu,

@@ -46,6 +46,11 @@ constexpr int kGroupM = 16;         // M-tiles per raster group
 #define FP8Q_BLOCK_BN 256
 #define FP8Q_BLOCK_WG 2
 #endif
+#ifndef FP8Q_TENSOR_BK
+#define FP8Q_TENSOR_BK 128
+#endif
+// K-block width of the per-tensor kernel at BN = 256 (64 -> a deeper ring).
+constexpr int kTensorBK = FP8Q_TENSOR_BK;
 constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
 constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 
@@ -73,10 +78,28 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nt = local / gsize;
 }
 
-template <int BN, int STAGES>
+// K-block width (bytes = FP8 elements) and its shared-memory swizzle: a
+// 128-byte K block uses 128-byte swizzling (8-row atoms of 1024 bytes), a
+// 64-byte K block 64-byte swizzling (8-row atoms of 512 bytes).
+template <int BK>
+struct Swz;
+template <>
+struct Swz<128> {
+  static constexpr uint32_t kMode = 2;
+  static constexpr uint32_t kSBO = 1024;
+  static constexpr CUtensorMapSwizzle kTma = CU_TENSOR_MAP_SWIZZLE_128B;
+};
+template <>
+struct Swz<64> {
+  static constexpr uint32_t kMode = 4;
+  static constexpr uint32_t kSBO = 512;
+  static constexpr CUtensorMapSwizzle kTma = CU_TENSOR_MAP_SWIZZLE_64B;
+};
+
+template <int BN, int STAGES, int BK = kBK>
 struct Layout {
-  static constexpr int kABytes = kBM * kBK;
-  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kABytes = kBM * BK;
+  static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kBarBytes = 8 * (2 * STAGES + 5);  // full, empty, acc full/empty x2, drain
@@ -84,11 +107,11 @@ struct Layout {
 };
 
 // Producer loop shared by both kernels.
-template <int BN, int STAGES>
+template <int BN, int STAGES, int BK = kBK>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUtensorMap *tb,
                                               const GemmArgs &p, uint32_t ring, uint32_t bars,
                                               volatile int *abort_flag) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, BK>;
   const int total = p.num_m_tiles * p.num_n_tiles;
   uint32_t it = 0;
   bool ok = true;
@@ -104,8 +127,8 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUten
       }
       const uint32_t sa = ring + s * L::kStageBytes;
       mbar_arrive_expect_tx(full, L::kStageBytes);
-      tma_load_2d(sa, ta, kb * kBK, mt * kBM, full);
-      tma_load_2d(sa + L::kABytes, tb, kb * kBK, nt * BN, full);
+      tma_load_2d(sa, ta, kb * BK, mt * kBM, full);
+      tma_load_2d(sa + L::kABytes, tb, kb * BK, nt * BN, full);
     }
   }
   if (!ok) {
@@ -121,17 +144,17 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUten
   }
 }
 
-// MMAs of one 128-byte K block held in ring slot `s`.
-template <int BN, int STAGES>
+// MMAs of one K block held in ring slot `s` (BK / 32 MMAs of K = 32).
+template <int BN, int STAGES, int BK = kBK>
 __device__ __forceinline__ void issue_kblock(uint32_t ring, uint32_t s, uint32_t d_tmem,
                                              uint32_t idesc, bool accumulate_first) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, BK>;
   const uint32_t a0 = ring + s * L::kStageBytes;
   const uint32_t b0 = a0 + L::kABytes;
 #pragma unroll
-  for (int k = 0; k < kBK / kUmmaK; ++k) {
-    const uint64_t ad = sdesc_k_sw128(a0 + k * kUmmaK);
-    const uint64_t bd = sdesc_k_sw128(b0 + k * kUmmaK);
+  for (int k = 0; k < BK / kUmmaK; ++k) {
+    const uint64_t ad = sdesc_k(a0 + k * kUmmaK, Swz<BK>::kSBO, Swz<BK>::kMode);
+    const uint64_t bd = sdesc_k(b0 + k * kUmmaK, Swz<BK>::kSBO, Swz<BK>::kMode);
     mma_f8f6f4(d_tmem, ad, bd, idesc, (accumulate_first || k > 0) ? 1u : 0u);
   }
 }
@@ -179,11 +202,11 @@ __device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n
 // ------------------------------------------------------------------------
 // Per-tensor scaled GEMM: 6 warps (producer, MMA, 4 epilogue warps).
 // ------------------------------------------------------------------------
-template <int BN, int STAGES, bool OUT_BF16>
+template <int BN, int STAGES, int BK, bool OUT_BF16>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap ta,
                        const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
-  using L = Layout<BN, STAGES>;
+  using L = Layout<BN, STAGES, BK>;
   constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // 128, 256 or 512
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -224,7 +247,7 @@ __global__ void __launch_bounds__(192, 1)
   const int total = p.num_m_tiles * p.num_n_tiles;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
+    if (lane == 0) producer_loop<BN, STAGES, BK>(&ta, &tb, p, ring, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
@@ -245,7 +268,7 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          issue_kblock<BN, STAGES>(ring, s, d_tmem, p.idesc, kb > 0);
+          issue_kblock<BN, STAGES, BK>(ring, s, d_tmem, p.idesc, kb > 0);
           mma_commit(empty0 + 8 * s);
         }
         if (!ok) break;
@@ -525,7 +548,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
 bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K, uint32_t box_k,
                uint32_t box_rows) {
   return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, box_k, box_rows,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
+                      box_k == 64 ? Swz<64>::kTma : Swz<128>::kTma);
 }
 
 template <typename KernelT>
@@ -533,11 +556,11 @@ cudaError_t set_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int BN, int STAGES, bool OUT_BF16>
+template <int BN, int STAGES, int BK, bool OUT_BF16>
 int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                cudaStream_t stream) {
-  using L = Layout<BN, STAGES>;
-  auto kernel = gemm_tensor_kernel<BN, STAGES, OUT_BF16>;
+  using L = Layout<BN, STAGES, BK>;
+  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16>;
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
@@ -615,9 +638,12 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   }
   int BN = kBlockScaledBN;
   if (tensor) BN = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
+  // Per-tensor scaling is free to pick its K-block width; tile/block scaling
+  // needs the 128-wide K blocks its scales are defined on.
+  const int BK = (tensor && BN == 256) ? kTensorBK : kBK;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, kBK, kBM) ||
-      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, kBK, (uint32_t)BN))
+  if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, (uint32_t)BK, kBM) ||
+      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)BK, (uint32_t)BN))
     return FP8Q_ERR_CUDA;
 
   GemmArgs a{};
@@ -626,7 +652,7 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   a.K = K;
   a.num_m_tiles = (int)((M + kBM - 1) / kBM);
   a.num_n_tiles = (int)((N + BN - 1) / BN);
-  a.num_k_blocks = (int)((K + kBK - 1) / kBK);
+  a.num_k_blocks = (int)((K + BK - 1) / BK);
   a.idesc = ptx::idesc_f8f6f4((uint32_t)A.format, (uint32_t)B.format, kBM, (uint32_t)BN);
   a.C = C;
   a.scale_a = A.scale;
@@ -644,13 +670,14 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
 
   if (tensor) {
     if (BN == 64)
-      return bf16 ? run_tensor<64, 8, true>(ta, tb, a, grid, stream)
-                  : run_tensor<64, 8, false>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<64, 8, 128, true>(ta, tb, a, grid, stream)
+                  : run_tensor<64, 8, 128, false>(ta, tb, a, grid, stream);
     if (BN == 128)
-      return bf16 ? run_tensor<128, 6, true>(ta, tb, a, grid, stream)
-                  : run_tensor<128, 6, false>(ta, tb, a, grid, stream);
-    return bf16 ? run_tensor<256, 4, true>(ta, tb, a, grid, stream)
-                : run_tensor<256, 4, false>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<128, 6, 128, true>(ta, tb, a, grid, stream)
+                  : run_tensor<128, 6, 128, false>(ta, tb, a, grid, stream);
+    constexpr int S256 = kTensorBK == 64 ? 9 : 4;   // ~216 KB or ~192 KB of ring
+    return bf16 ? run_tensor<256, S256, kTensorBK, true>(ta, tb, a, grid, stream)
+                : run_tensor<256, S256, kTensorBK, false>(ta, tb, a, grid, stream);
   }
   const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
   constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;

@@ -164,6 +164,19 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for a swizzle mode / 8-row stride given explicitly (mode 2 with
+// 1024-byte SBO: 128-byte swizzle; mode 4 with 512-byte SBO: 64-byte
+// swizzle, rows of 64 bytes).
+__device__ __forceinline__ uint64_t sdesc_k(uint32_t saddr, uint32_t sbo, uint32_t mode) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(mode) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f8f6f4, dense, fp32 accumulator, both
 // operands K-major: D format in [4,6) (1 = f32), A format in [7,10), B format
 // in [10,13) (0 = E4M3, 1 = E5M2), N >> 3 in [17,23), M >> 4 in [24,29).

@@ -27,6 +27,7 @@ IN_BF16 = 1
 SCALE_TENSOR = 0
 SCALE_TILE = 1
 SCALE_BLOCK = 2
+SCALE_ROW = 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
@@ -78,6 +79,7 @@ def _load():
             "orc_quantize_tile_cols": (None, [P, I32, I64, I64, I32, I32, P, P]),
             "orc_quantize_block": (None, [P, I32, I64, I64, I32, I32, P, P, P]),
             "orc_quantize_delayed": (F32, [P, I32, I64, I64, I32, I32, P, I32, P, P, P]),
+            "orc_quantize_rowwise": (None, [P, I32, I64, I64, I32, I32, P, P, P, P]),
             "orc_dequantize": (None, [P, I64, I32, F32, P]),
             "orc_operand_scale": (F32, [ctypes.POINTER(Operand), I64, I64]),
             "orc_gemm_points": (None, [ctypes.POINTER(Operand), ctypes.POINTER(Operand),
@@ -212,6 +214,20 @@ def quantize_block(x: np.ndarray, fmt: int, saturate=False, want_q=True, want_qt
     return q, qt, sc
 
 
+def quantize_rowwise(x: np.ndarray, fmt: int, rows=True, cols=False, saturate=False):
+    """Row-wise scaling.  Returns (q [R,C], q_scales [R], q_t [C,R], qt_scales [C]),
+    with None for the pair not requested."""
+    x, dt = _input(x)
+    R, C = x.shape
+    q = np.empty((R, C), np.uint8) if rows else None
+    qs = np.empty(R, np.float32) if rows else None
+    qt = np.empty((C, R), np.uint8) if cols else None
+    qts = np.empty(C, np.float32) if cols else None
+    _load().orc_quantize_rowwise(_ptr(x), dt, R, C, fmt, int(saturate), _ptr(q), _ptr(qs),
+                                 _ptr(qt), _ptr(qts))
+    return q, qs, qt, qts
+
+
 def quantize_delayed(x: np.ndarray, fmt: int, history: np.ndarray, next_slot: int,
                      saturate=False, want_q=True, want_qt=False):
     """Returns (q, q_t, s, new_history, new_next)."""
@@ -259,6 +275,11 @@ class GemmOperand:
     def tile(cls, q, fmt, scales):
         """1x128 tiles with scales laid out [ceil(K/128), rows]."""
         return cls(q, fmt, SCALE_TILE, scales, stride_row=1, stride_k=q.shape[0])
+
+    @classmethod
+    def row(cls, q, fmt, scales):
+        """One scale per row over all of K (scales [rows])."""
+        return cls(q, fmt, SCALE_ROW, scales, stride_row=1, stride_k=0)
 
     @classmethod
     def block(cls, q, fmt, scales, transposed=False):

@@ -250,6 +250,45 @@ void orc_quantize_block(const void *x, int in_dtype, int64_t rows,
     }
 }
 
+/* Row-wise scaling: scaled_roundtrip applied to each whole row (and, for the
+ * transposed copy, to each whole column). */
+void orc_quantize_rowwise(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, int saturate, uint8_t *q,
+                          float *q_scales, uint8_t *q_t, float *qt_scales) {
+  if (q) {
+    for (int64_t r = 0; r < rows; ++r) {
+      float amax = 0.0f;
+      int nan_seen = 0;
+      for (int64_t c = 0; c < cols; ++c) {
+        float a = fabsf(orc_load(x, in_dtype, r * cols + c));
+        if (isnan(a)) nan_seen = 1;
+        else if (a > amax) amax = a;
+      }
+      if (nan_seen) amax = NAN;
+      float s = orc_scale_from_amax(amax, fmt);
+      q_scales[r] = s;
+      for (int64_t c = 0; c < cols; ++c)
+        q[r * cols + c] = cast_one(orc_load(x, in_dtype, r * cols + c), s, fmt, saturate);
+    }
+  }
+  if (q_t) {
+    for (int64_t c = 0; c < cols; ++c) {
+      float amax = 0.0f;
+      int nan_seen = 0;
+      for (int64_t r = 0; r < rows; ++r) {
+        float a = fabsf(orc_load(x, in_dtype, r * cols + c));
+        if (isnan(a)) nan_seen = 1;
+        else if (a > amax) amax = a;
+      }
+      if (nan_seen) amax = NAN;
+      float s = orc_scale_from_amax(amax, fmt);
+      qt_scales[c] = s;
+      for (int64_t r = 0; r < rows; ++r)
+        q_t[c * rows + r] = cast_one(orc_load(x, in_dtype, r * cols + c), s, fmt, saturate);
+    }
+  }
+}
+
 /* Delayed scaling ([fp8_parity] smoke step 3; [te_blog] "FP8 DelayedScaling
  * ... relies on an amax history"): the scale comes from the history only, so
  * the tensor being cast does not see its own amax; its amax is recorded for
@@ -284,6 +323,7 @@ float orc_operand_scale(const orc_operand *op, int64_t row, int64_t k) {
   if (op->scaling == ORC_SCALE_TENSOR) return op->scale[0];
   if (op->scaling == ORC_SCALE_TILE)
     return op->scale[kb * op->stride_k + row * op->stride_row];
+  if (op->scaling == ORC_SCALE_ROW) return op->scale[row * op->stride_row];
   return op->scale[(row / 128) * op->stride_row + kb * op->stride_k];
 }
 

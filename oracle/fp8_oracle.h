@@ -51,6 +51,7 @@ extern "C" {
 #define ORC_SCALE_TENSOR 0
 #define ORC_SCALE_TILE 1   /* one scale per row per 128-wide K block */
 #define ORC_SCALE_BLOCK 2  /* one scale per 128x128 block            */
+#define ORC_SCALE_ROW 3    /* one scale per row over all of K         */
 
 double orc_fmax(int fmt);
 
@@ -103,6 +104,17 @@ void orc_quantize_block(const void *x, int in_dtype, int64_t rows,
                         int64_t cols, int fmt, int saturate, uint8_t *q,
                         uint8_t *q_t, float *scales);
 
+/* Row-wise scaling (the fp8_parity page's torchao "rowwise" recipe, read as
+ * one scale per row of each K-major GEMM operand): either or both of
+ *   q [rows, cols] with q_scales[rows]: row r scaled by its own amax over
+ *     all columns;
+ *   q_t [cols, rows] with qt_scales[cols]: column c of x (row c of x^T)
+ *     scaled by its own amax over all rows.
+ * Each pair may be NULL. */
+void orc_quantize_rowwise(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, int saturate, uint8_t *q,
+                          float *q_scales, uint8_t *q_t, float *qt_scales);
+
 /* Delayed scaling with an amax history ring of hist_len entries.
  * s = max(history) / fmax (clamped as orc_scale_from_amax); x is cast with s;
  * then amax(x) overwrites history[*next] and *next advances modulo hist_len.
@@ -119,6 +131,7 @@ void orc_dequantize(const uint8_t *q, int64_t n, int fmt, float s, float *d);
  *   TENSOR: scale[0]
  *   TILE:   scale[kb * stride_k + row * stride_row]
  *   BLOCK:  scale[(row / 128) * stride_row + kb * stride_k]
+ *   ROW:    scale[row * stride_row]
  * with kb = k / 128. */
 typedef struct {
   const uint8_t *data;

@@ -479,3 +479,44 @@ def test_fp8matmul_roles_vs_page_torch():
         r = ref[role].double().numpy()
         assert y.shape == r.shape
         assert np.all(np.abs(y - r) <= 1e-6 * ab + 1e-12), role
+
+
+# ---------------------------------------------------------------- row-wise
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_rowwise_is_page_roundtrip_per_row_and_column(fmt):
+    """Row-wise scaling applies the page's scaled_roundtrip to each whole row
+    (and to each whole column for the transposed copy)."""
+    rng = np.random.default_rng(30)
+    x = (rng.standard_normal((40, 352)) * rng.choice([1e-2, 1, 50], size=(40, 1))).astype(np.float32)
+    x[3, :] = 0.0
+    q, qs, qt, qts = oracle.quantize_rowwise(x, fmt, rows=True, cols=True)
+    for r in range(x.shape[0]):
+        qb, sb = _page_roundtrip_torch(torch.from_numpy(x[r].copy()), FMT[fmt], oracle.fmax(fmt))
+        assert qs[r] == sb.item() and np.array_equal(q[r], qb.numpy())
+    for c in range(x.shape[1]):
+        qb, sb = _page_roundtrip_torch(torch.from_numpy(x[:, c].copy()), FMT[fmt],
+                                       oracle.fmax(fmt))
+        assert qts[c] == sb.item() and np.array_equal(qt[c], qb.numpy())
+
+
+def test_rowwise_equals_tiles_when_a_row_is_one_tile():
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((64, 128)) * 3).astype(np.float32)
+    q, qs, _, _ = oracle.quantize_rowwise(x, oracle.E4M3)
+    q2, s2 = oracle.quantize_tile_rows(x, oracle.E4M3)
+    assert np.array_equal(q, q2) and np.array_equal(qs, s2[0])
+
+
+def test_gemm_row_scales_vs_numpy():
+    rng = np.random.default_rng(32)
+    M, N, K = 70, 90, 260
+    A = _rand_codes(rng, (M, K), oracle.E4M3)
+    B = _rand_codes(rng, (N, K), oracle.E5M2)
+    sa = rng.uniform(0.1, 2, M).astype(np.float32)
+    sb = rng.uniform(0.1, 2, N).astype(np.float32)
+    y, ab = oracle.gemm_rows(oracle.GemmOperand.row(A, oracle.E4M3, sa),
+                             oracle.GemmOperand.row(B, oracle.E5M2, sb))
+    ref = (oracle.decode_table(oracle.E4M3)[A] * sa[:, None].astype(np.float64)) @ \
+          (oracle.decode_table(oracle.E5M2)[B] * sb[:, None].astype(np.float64)).T
+    assert np.all(np.abs(y - ref) <= 1e-13 * ab + 1e-300)

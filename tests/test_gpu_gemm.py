@@ -305,3 +305,55 @@ def test_linear_autocast_matches_steps(fq):
     y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tensor(qx, 0, sx), fq.GemmOperand.tensor(qw, 0, sw))
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     assert hx.state()[1] == 1 and hw.state()[1] == 1
+
+
+def test_layer_dgrad_wgrad_full_size_delayed_vs_current(fq):
+    """Attention-out layer at full size, grad_out ~ N(0, 1e-3) with 40.0 spikes
+    (E5M2): current scaling represents the spikes exactly, delayed scaling
+    (history of spike-free draws) turns them into Inf; bytes and scales match
+    the oracle in both, and Dgrad / Wgrad match it on sampled outputs."""
+    idx = 1
+    shape = workloads.LAYER[idx]
+    x, w, g = workloads.layer_inputs(shape, idx)
+    M, K, N = x.shape[0], shape.K, shape.N
+    xd, wd, gd = x.cuda(), w.cuda(), g.cuda()
+    xo, wo, go = to_oracle(x), to_oracle(w), to_oracle(g)
+    hist0 = [float(oracle.amax(to_oracle(d))) for d in workloads.history_draws((M, N))]
+    qx, qxt, sx = fq.fp8_quantize_tensor(xd, 0, fq.fp8_amax(xd), want_qt=True)
+    qw, qwt, sw = fq.fp8_quantize_tensor(wd, 0, fq.fp8_amax(wd), want_qt=True)
+    rx, rxt, rsx = oracle.quantize_tensor(xo, 0, want_qt=True)
+    rw, rwt, rsw = oracle.quantize_tensor(wo, 0, want_qt=True)
+    assert_bytes_equal(u8(qxt), rxt, "x_t")
+    assert_bytes_equal(u8(qwt), rwt, "w_t")
+    spike = go == np.uint16(0x4220)           # 40.0 in bf16
+    assert spike.sum() == (M * N) // 10 ** 6
+    T, R = fq.GemmOperand.tensor, oracle.GemmOperand.tensor
+    rng = np.random.default_rng(4)
+    for mode in ("current", "delayed"):
+        if mode == "current":
+            qg, qgt, sg = fq.fp8_quantize_tensor(gd, 1, fq.fp8_amax(gd), want_qt=True)
+            rg, rgt, rsg = oracle.quantize_tensor(go, 1, want_qt=True)
+        else:
+            h = fq.History(initial=hist0)
+            qg, qgt, sg = fq.fp8_quantize_delayed(gd, 1, h, want_qt=True)
+            rg, rgt, rsg, rh, _ = oracle.quantize_delayed(go, 1, hist0, 0, want_qt=True)
+            assert_f32_bits_equal(np.array(h.state()[0], np.float32), rh, "history")
+        assert_f32_bits_equal(f32(sg), np.array([rsg], np.float32), f"{mode} scale")
+        assert_bytes_equal(u8(qg), rg, f"{mode} g")
+        assert_bytes_equal(u8(qgt), rgt, f"{mode} g_t")
+        codes = u8(qg)[spike]
+        if mode == "current":
+            assert np.all(codes == 0x7B)          # 40 / s = 57344 exactly: the largest E5M2
+        else:
+            assert np.all(codes == 0x7C)          # overflow -> +Inf
+            continue                               # Inf operands: the GEMM output is not finite
+        dx = fq.fp8_gemm_dgrad(T(qg, 1, sg), T(qwt, 0, sw))
+        dw = fq.fp8_gemm_wgrad(T(qgt, 1, sg), T(qxt, 0, sx))
+        gpu_status_ok(fq)
+        for got, opA, opB, Rr, Cc, nm in [
+            (dx, R(rg, 1, rsg), R(rwt, 0, rsw), M, K, "dgrad"),
+            (dw, R(rgt, 1, rsg), R(rxt, 0, rsx), N, K, "wgrad"),
+        ]:
+            ms, ns = _sample_points(Rr, Cc, rng, n=2048)
+            yr, ab = oracle.gemm_points(opA, opB, ms, ns)
+            check_bound(f32(got)[ms, ns], yr, ab, True, f"{mode} {nm}")

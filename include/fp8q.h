@@ -80,7 +80,8 @@ typedef enum fp8q_format {
 typedef enum fp8q_scaling {
   FP8Q_SCALE_TENSOR = 0,      /* one scale for the whole operand */
   FP8Q_SCALE_TILE_1x128 = 1,  /* one scale per row per 128-wide K block */
-  FP8Q_SCALE_BLOCK_128x128 = 2 /* one scale per 128x128 block */
+  FP8Q_SCALE_BLOCK_128x128 = 2, /* one scale per 128x128 block */
+  FP8Q_SCALE_ROW = 3            /* one scale per row over all of K */
 } fp8q_scaling;
 
 typedef enum fp8q_recipe {
@@ -197,6 +198,22 @@ int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows,
                            float *q_scales, uint8_t *q_t, float *qt_scales,
                            int saturate, cudaStream_t stream);
 
+/* Row-wise scaling, the torchao "rowwise" recipe the fp8_parity page offers
+ * (argument --recipe), read as one scale per row of each K-major GEMM operand
+ * over its whole contraction: from two reads of x, either or both of
+ *   q [rows, cols] with q_scales [rows]: row r cast with its own scale;
+ *   q_t [cols, rows] with qt_scales [cols]: column c of x (row c of x^T) cast
+ *     with its own scale (what Dgrad's and Wgrad's operands need).
+ * Scales as everywhere: max(fl32(amax / fmax), 1e-12).  cols % 16 == 0;
+ * rows % 16 == 0 when the column pair is requested.  Each pair is
+ * both-or-neither; at least one.  The scale arrays also serve as the amax
+ * accumulators of the first read (the call zeroes them on `stream`).
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_rowwise(const void *x, int in_dtype, int64_t rows,
+                         int64_t cols, int format, uint8_t *q, float *q_scales,
+                         uint8_t *q_t, float *qt_scales, int saturate,
+                         cudaStream_t stream);
+
 /* 128x128 block scaling for weights ([te_blog] "2D block scaling for
  * weights"): one scale per block, block_scales [ceil(rows/128),
  * ceil(cols/128)] row-major; q [rows, cols] and/or q_t [cols, rows] (the same
@@ -216,6 +233,7 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows,
  *   FP8Q_SCALE_TENSOR:        scale[0]
  *   FP8Q_SCALE_TILE_1x128:    scale[kb * scale_stride_k + row * scale_stride_row]
  *   FP8Q_SCALE_BLOCK_128x128: scale[(row/128) * scale_stride_row + kb * scale_stride_k]
+ *   FP8Q_SCALE_ROW:           scale[row * scale_stride_row]
  * (scale in device memory).  The quantize calls above produce:
  *   tile scales of an [R, K] matrix:   stride_row = 1, stride_k = R
  *   block scales of an [R, K] matrix:  stride_row = ceil(K/128), stride_k = 1
@@ -238,8 +256,10 @@ typedef struct fp8q_operand {
  * that block's scale product.
  *   A: [M, K], B: [N, K]; N % 16 == 0, K % 16 == 0; M >= 0 any.
  *   M == 0 or N == 0: nothing to do.  K == 0: C is zero.
- * Errors: INVALID_ARG, MISALIGNED, ARCH, NOT_IMPLEMENTED (a TILE/BLOCK
- * combination outside: A TILE with B TILE or BLOCK), CUDA. */
+ * Supported combinations: TENSOR/ROW with TENSOR/ROW (scales applied in the
+ * epilogue), and A TILE with B TILE or BLOCK (promoted per K block).
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, NOT_IMPLEMENTED (other combinations),
+ * CUDA. */
 int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C,
              int out_dtype, int64_t M, int64_t N, int64_t K,
              cudaStream_t stream);

@@ -27,6 +27,7 @@ DT_BF16 = 1
 SCALE_TENSOR = 0
 SCALE_TILE_1x128 = 1
 SCALE_BLOCK_128x128 = 2
+SCALE_ROW = 3
 RECIPE_TENSOR_CURRENT = 0
 RECIPE_TENSOR_DELAYED = 1
 RECIPE_BLOCK = 2
@@ -45,7 +46,8 @@ EXPORTS = (
     "fp8q_status_string", "fp8q_device_status", "fp8q_device_supported",
     "fp8q_selftest_barrier_timeout", "fp8_amax",
     "fp8_quantize_tensor", "fp8_quantize_delayed", "fp8q_history_init",
-    "fp8_quantize_tile1x128", "fp8_quantize_block128x128", "fp8_gemm", "fp8_gemm_fprop",
+    "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_block128x128", "fp8_gemm",
+    "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
     "fp8_linear_autocast_noalloc",
 )
@@ -91,6 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8_quantize_delayed": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8q_history_init": (I32, [P, P, P]),
             "fp8_quantize_tile1x128": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+            "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_block128x128": (I32, [P, I32, I64, I64, I32, P, P, P, I32, P]),
             "fp8_gemm": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
@@ -254,6 +257,25 @@ def fp8_quantize_tile1x128(x, fmt, rows=True, cols=False, saturate=False, q=None
     return ((q, q_scales) if rows else (None, None)) + ((q_t, qt_scales) if cols else (None, None))
 
 
+def fp8_quantize_rowwise(x, fmt, rows=True, cols=False, saturate=False, q=None, q_scales=None,
+                         q_t=None, qt_scales=None, stream=None):
+    """Row-wise scaling: q [R,C] with q_scales [R] (one scale per row) and/or
+    q_t [C,R] with qt_scales [C] (one scale per column of x)."""
+    R, C = _rows_cols(x)
+    if rows:
+        q = q if q is not None else _empty((R, C), torch.uint8, x)
+        q_scales = q_scales if q_scales is not None else _empty((R,), torch.float32, x)
+    if cols:
+        q_t = q_t if q_t is not None else _empty((C, R), torch.uint8, x)
+        qt_scales = qt_scales if qt_scales is not None else _empty((C,), torch.float32, x)
+    _check(lib().fp8_quantize_rowwise(
+        _ptr(x), _in_dtype(x), R, C, fmt, _ptr(q if rows else None),
+        _ptr(q_scales if rows else None), _ptr(q_t if cols else None),
+        _ptr(qt_scales if cols else None), int(saturate), _stream(stream)),
+        "fp8_quantize_rowwise")
+    return ((q, q_scales) if rows else (None, None)) + ((q_t, qt_scales) if cols else (None, None))
+
+
 def fp8_quantize_block128x128(x, fmt, want_q=True, want_qt=False, saturate=False, q=None,
                               q_t=None, scales=None, stream=None):
     R, C = _rows_cols(x)
@@ -294,6 +316,11 @@ class GemmOperand:
     def tile(cls, q, fmt, scales):
         """scales [ceil(K/128), rows] as written by fp8_quantize_tile1x128."""
         return cls(q, fmt, SCALE_TILE_1x128, scales, 1, q.shape[0])
+
+    @classmethod
+    def row(cls, q, fmt, scales):
+        """One scale per row over all of K (scales [rows])."""
+        return cls(q, fmt, SCALE_ROW, scales, 1, 0)
 
     @classmethod
     def block(cls, q, fmt, scales):

@@ -88,7 +88,7 @@ int check_ptr(const void *p, bool required) {
 int check_operand(const fp8q_operand *op, int64_t rows, int64_t K) {
   if (op == nullptr || !valid_format(op->format)) return FP8Q_ERR_INVALID_ARG;
   if (op->scaling != FP8Q_SCALE_TENSOR && op->scaling != FP8Q_SCALE_TILE_1x128 &&
-      op->scaling != FP8Q_SCALE_BLOCK_128x128)
+      op->scaling != FP8Q_SCALE_BLOCK_128x128 && op->scaling != FP8Q_SCALE_ROW)
     return FP8Q_ERR_INVALID_ARG;
   if (op->scale == nullptr) return FP8Q_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(op->scale) & 3u) != 0) return FP8Q_ERR_MISALIGNED;
@@ -302,6 +302,52 @@ int fp8_quantize_tile1x128(const void *x, int in_dtype, int64_t rows, int64_t co
     fprintf(stderr, "[fp8q] quantize_tile1x128 %lldx%lld fmt=%d rows=%d cols=%d\n",
             (long long)rows, (long long)cols, format, want_row, want_col);
   return from_cuda(launch_quant2d(p, stream));
+}
+
+int fp8_quantize_rowwise(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                         uint8_t *q, float *q_scales, uint8_t *q_t, float *qt_scales,
+                         int saturate, cudaStream_t stream) {
+  const bool want_row = q != nullptr || q_scales != nullptr;
+  const bool want_col = q_t != nullptr || qt_scales != nullptr;
+  int rc = check_quant(x, in_dtype, rows, cols, format, want_col);
+  if (rc != FP8Q_OK) return rc;
+  if (rows > 0 && cols > 0) {
+    if (!want_row && !want_col) return FP8Q_ERR_INVALID_ARG;
+    if (want_row && (q == nullptr || q_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+    if (want_col && (q_t == nullptr || qt_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  }
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if ((q_scales && (reinterpret_cast<uintptr_t>(q_scales) & 3u)) ||
+      (qt_scales && (reinterpret_cast<uintptr_t>(qt_scales) & 3u)))
+    return FP8Q_ERR_MISALIGNED;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  if (rows == 0 || cols == 0) return FP8Q_OK;
+  // pass 1 gathers the amaxes in the scale arrays, so they start at zero
+  if (want_row && cudaMemsetAsync(q_scales, 0, sizeof(float) * (size_t)rows, stream) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  if (want_col && cudaMemsetAsync(qt_scales, 0, sizeof(float) * (size_t)cols, stream) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.err = device_error_word();
+  p.q_scales = want_row ? q_scales : nullptr;
+  p.qt_scales = want_col ? qt_scales : nullptr;
+  p.mode = kModeRowAmax;
+  if ((rc = from_cuda(launch_quant2d(p, stream))) != FP8Q_OK) return rc;
+  p.mode = kModeRowCast;
+  p.q = want_row ? q : nullptr;
+  p.q_t = want_col ? q_t : nullptr;
+  if ((rc = from_cuda(launch_quant2d(p, stream))) != FP8Q_OK) return rc;
+  if (want_row && (rc = from_cuda(launch_amax_to_scale(q_scales, rows, format, stream))) != FP8Q_OK)
+    return rc;
+  if (want_col && (rc = from_cuda(launch_amax_to_scale(qt_scales, cols, format, stream))) != FP8Q_OK)
+    return rc;
+  return FP8Q_OK;
 }
 
 int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t cols,

@@ -62,9 +62,10 @@ struct GemmArgs {
   // per-tensor scales (device scalars)
   const float *scale_a;
   const float *scale_b;
-  // tile / block scales
+  // tile / block / row scales
   int64_t a_stride_row, a_stride_k;
   int64_t b_stride_row, b_stride_k;
+  int a_row, b_row;   // per-tensor kernel: 1 = one scale per row (ROW), 0 = scalar
   unsigned int *err;
 };
 
@@ -202,7 +203,7 @@ __device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n
 // ------------------------------------------------------------------------
 // Per-tensor scaled GEMM: 6 warps (producer, MMA, 4 epilogue warps).
 // ------------------------------------------------------------------------
-template <int BN, int STAGES, int BK, bool OUT_BF16>
+template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap ta,
                        const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
@@ -280,7 +281,9 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // Epilogue warps 2..5 -> TMEM lane quarters 2, 3, 0, 1.
     const int quarter = warp & 3;
-    const float scale = __fmul_rn(p.scale_a[0], p.scale_b[0]);
+    // Per-tensor: one product s_A s_B.  With row scales (VEC): s_A of this
+    // thread's row times s_B of each column, applied the same way.
+    const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
     uint32_t acc_it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++acc_it) {
       int mt, nt;
@@ -289,15 +292,27 @@ __global__ void __launch_bounds__(192, 1)
       if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
       tc_fence_after();
       const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
+      float sa = 0.0f;
+      if (VEC)
+        sa = p.a_row ? (m < p.M ? p.scale_a[m * p.a_stride_row] : 0.0f) : p.scale_a[0];
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + c * 32, r);
         tmem_ld_wait();
         float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
         const int64_t n0 = (int64_t)nt * BN + c * 32;
+        if (VEC) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float sb = p.b_row ? (n0 + j < p.N ? p.scale_b[(n0 + j) * p.b_stride_row] : 0.0f)
+                                     : p.scale_b[0];
+            v[j] = __fmul_rn(__uint_as_float(r[j]), __fmul_rn(sa, sb));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
+        }
         if (m < p.M && n0 < p.N) store32<OUT_BF16>(p.C, p.N, m, n0, v);
       }
       tc_fence_before();
@@ -556,11 +571,11 @@ cudaError_t set_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int BN, int STAGES, int BK, bool OUT_BF16>
+template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC>
 int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                cudaStream_t stream) {
   using L = Layout<BN, STAGES, BK>;
-  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16>;
+  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16, VEC>;
   static bool attr_done = false;  // per instantiation
   if (!attr_done) {
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
@@ -630,7 +645,12 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
                ? FP8Q_OK
                : FP8Q_ERR_CUDA;
   }
-  const bool tensor = A.scaling == FP8Q_SCALE_TENSOR && B.scaling == FP8Q_SCALE_TENSOR;
+  // TENSOR and ROW scales are constant along K: the whole sum accumulates in
+  // TMEM and the scales are applied in the epilogue.
+  const bool a_ep = A.scaling == FP8Q_SCALE_TENSOR || A.scaling == FP8Q_SCALE_ROW;
+  const bool b_ep = B.scaling == FP8Q_SCALE_TENSOR || B.scaling == FP8Q_SCALE_ROW;
+  const bool tensor = a_ep && b_ep;
+  const bool vec = tensor && (A.scaling == FP8Q_SCALE_ROW || B.scaling == FP8Q_SCALE_ROW);
   if (!tensor) {
     if (A.scaling != FP8Q_SCALE_TILE_1x128 ||
         (B.scaling != FP8Q_SCALE_TILE_1x128 && B.scaling != FP8Q_SCALE_BLOCK_128x128))
@@ -661,6 +681,8 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   a.a_stride_k = A.stride_k;
   a.b_stride_row = B.stride_row;
   a.b_stride_k = B.stride_k;
+  a.a_row = A.scaling == FP8Q_SCALE_ROW ? 1 : 0;
+  a.b_row = B.scaling == FP8Q_SCALE_ROW ? 1 : 0;
   a.err = device_error_word();
   if (a.err == nullptr) return FP8Q_ERR_CUDA;
   const int64_t tiles = (int64_t)a.num_m_tiles * a.num_n_tiles;
@@ -669,15 +691,25 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   if (tiles < grid) grid = (int)tiles;
 
   if (tensor) {
-    if (BN == 64)
-      return bf16 ? run_tensor<64, 8, 128, true>(ta, tb, a, grid, stream)
-                  : run_tensor<64, 8, 128, false>(ta, tb, a, grid, stream);
-    if (BN == 128)
-      return bf16 ? run_tensor<128, 6, 128, true>(ta, tb, a, grid, stream)
-                  : run_tensor<128, 6, 128, false>(ta, tb, a, grid, stream);
     constexpr int S256 = kTensorBK == 64 ? 9 : 4;   // ~216 KB or ~192 KB of ring
-    return bf16 ? run_tensor<256, S256, kTensorBK, true>(ta, tb, a, grid, stream)
-                : run_tensor<256, S256, kTensorBK, false>(ta, tb, a, grid, stream);
+    if (vec) {
+      if (BN == 64)
+        return bf16 ? run_tensor<64, 8, 128, true, true>(ta, tb, a, grid, stream)
+                    : run_tensor<64, 8, 128, false, true>(ta, tb, a, grid, stream);
+      if (BN == 128)
+        return bf16 ? run_tensor<128, 6, 128, true, true>(ta, tb, a, grid, stream)
+                    : run_tensor<128, 6, 128, false, true>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<256, S256, kTensorBK, true, true>(ta, tb, a, grid, stream)
+                  : run_tensor<256, S256, kTensorBK, false, true>(ta, tb, a, grid, stream);
+    }
+    if (BN == 64)
+      return bf16 ? run_tensor<64, 8, 128, true, false>(ta, tb, a, grid, stream)
+                  : run_tensor<64, 8, 128, false, false>(ta, tb, a, grid, stream);
+    if (BN == 128)
+      return bf16 ? run_tensor<128, 6, 128, true, false>(ta, tb, a, grid, stream)
+                  : run_tensor<128, 6, 128, false, false>(ta, tb, a, grid, stream);
+    return bf16 ? run_tensor<256, S256, kTensorBK, true, false>(ta, tb, a, grid, stream)
+                : run_tensor<256, S256, kTensorBK, false, false>(ta, tb, a, grid, stream);
   }
   const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
   constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;

@@ -29,7 +29,9 @@ enum QuantMode : int {
   kModeTensorCurrent = 0,  // s from a device amax
   kModeTensorDelayed = 1,  // s from a device amax history, amax(x) pushed
   kModeTile = 2,           // 1x128 row tiles and/or 128x1 column tiles
-  kModeBlock = 3           // 128x128 blocks
+  kModeBlock = 3,          // 128x128 blocks
+  kModeRowAmax = 4,        // row-wise pass 1: per-row / per-column amax into the scale arrays
+  kModeRowCast = 5         // row-wise pass 2: cast with per-row / per-column scales
 };
 
 struct QuantParams {
@@ -52,6 +54,8 @@ struct QuantParams {
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
                         cudaStream_t stream);
 cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream);
+// Row-wise pass 3: s[i] = max(fl32(s[i] / fmax), 1e-12) in place.
+cudaError_t launch_amax_to_scale(float *s, int64_t n, int format, cudaStream_t stream);
 
 struct GemmOperandDev {
   const uint8_t *data;

@@ -306,7 +306,10 @@ enum KernelMode : int {
   kKTileRow = 2,    // 1x128 row tiles -> q, q_scales
   kKTileCol = 3,    // 128x1 column tiles -> q_t, qt_scales
   kKTileBoth = 4,   // both from one read
-  kKBlock = 5       // 128x128 blocks -> q and/or q_t, block scales
+  kKBlock = 5,      // 128x128 blocks -> q and/or q_t, block scales
+  kKRowAmax = 6,    // row-wise pass 1: per-row / per-column amax, atomicMax into
+                    // q_scales / qt_scales (as fp32 bit patterns)
+  kKRowCast = 7     // row-wise pass 2: cast with the scales of those amaxes
 };
 
 // Input tiles (128 x 128 elements) reach shared memory by TMA through a ring
@@ -325,6 +328,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     quant2d_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr bool kRowTiles = (KM == kKTileRow || KM == kKTileBoth);
   constexpr bool kColTiles = (KM == kKTileCol || KM == kKTileBoth);
+  constexpr bool kRowwise = (KM == kKRowAmax || KM == kKRowCast);
   constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock);
   using Ring = QuantRing<InT>;
   const float fm = FmtTraits<FMT>::kMax;
@@ -431,11 +435,11 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     uint32_t rowmax[8];
     uint32_t cmp[Row8<InT>::kColWords];
     uint32_t tmax = 0;
-    if (kRowTiles || kUniform) {
+    if (kRowTiles || kUniform || kRowwise) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) rowmax[i] = v[i].absmax_bits();
     }
-    if (kColTiles) {
+    if (kColTiles || kRowwise) {
 #pragma unroll
       for (int k = 0; k < Row8<InT>::kColWords; ++k) cmp[k] = 0;
 #pragma unroll
@@ -554,6 +558,93 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
 #pragma unroll
           for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
           uint2 b = cast8<FMT>(cv, s, r, fast_ok<FMT>(colmax[j], r), saturate);
+          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = b;
+        }
+      }
+    }
+    // ------------------------------------------- row-wise scaling, pass 1
+    if (KM == kKRowAmax) {
+      if (p.q_scales != nullptr) {
+        // same half-warp butterfly as the 1x128 rows, then one atomicMax per row
+        const bool h3 = cg & 8, h2 = cg & 4, h1 = cg & 2;
+        uint32_t a4[4];
+#pragma unroll
+        for (int t4 = 0; t4 < 4; ++t4) {
+          uint32_t keep = h3 ? rowmax[t4 + 4] : rowmax[t4];
+          uint32_t send = h3 ? rowmax[t4] : rowmax[t4 + 4];
+          a4[t4] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 8));
+        }
+        uint32_t a2[2];
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+          uint32_t keep = h2 ? a4[t2 + 2] : a4[t2];
+          uint32_t send = h2 ? a4[t2] : a4[t2 + 2];
+          a2[t2] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, 4));
+        }
+        uint32_t a1 = max(h1 ? a2[1] : a2[0], __shfl_xor_sync(0xFFFFFFFFu, h1 ? a2[0] : a2[1], 2));
+        a1 = max(a1, __shfl_xor_sync(0xFFFFFFFFu, a1, 1));
+        const int rsel = (h3 ? 4 : 0) + (h2 ? 2 : 0) + (h1 ? 1 : 0);
+        if ((cg & 1) == 0 && rbase + rsel < rows)
+          atomicMax(reinterpret_cast<unsigned int *>(p.q_scales) + rbase + rsel, a1);
+      }
+      if (p.qt_scales != nullptr) {
+        uint32_t colmax[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          colmax[j] = Row8<InT>::colmax_bits(cmp, j);
+          colmax[j] = max(colmax[j], __shfl_xor_sync(0xFFFFFFFFu, colmax[j], 16));
+        }
+        if (lane < 16) {
+          *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8]) =
+              make_uint4(colmax[0], colmax[1], colmax[2], colmax[3]);
+          *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8 + 4]) =
+              make_uint4(colmax[4], colmax[5], colmax[6], colmax[7]);
+        }
+        __syncthreads();
+        if (tid < 128 && c0 + tid < cols) {
+          uint32_t m = sh_colmax[0][tid];
+#pragma unroll
+          for (int w = 1; w < 8; ++w) m = max(m, sh_colmax[w][tid]);
+          atomicMax(reinterpret_cast<unsigned int *>(p.qt_scales) + c0 + tid, m);
+        }
+      }
+    }
+
+    // ------------------------------------------- row-wise scaling, pass 2
+    if (KM == kKRowCast) {
+      // scales of this tile's 128 rows / 128 columns from the pass-1 amaxes
+      if (tid < 128) {
+        if (p.q_scales != nullptr) {
+          const float a = (r0 + tid < rows) ? p.q_scales[r0 + tid] : 0.0f;
+          const float sr = scale_from_amax(a, fm);
+          sh_row_s[tid] = sr;
+          sh_row_r[tid] = __fdiv_rn(1.0f, sr);
+        }
+        if (p.qt_scales != nullptr) {
+          const float a = (c0 + tid < cols) ? p.qt_scales[c0 + tid] : 0.0f;
+          const float sc = scale_from_amax(a, fm);
+          sh_col_s[tid] = sc;
+          sh_col_r[tid] = __fdiv_rn(1.0f, sc);
+        }
+      }
+      __syncthreads();
+      if (p.q_scales != nullptr && col_ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float sr = sh_row_s[rg * 8 + i], rr = sh_row_r[rg * 8 + i];
+          uint2 b = cast_row<FMT>(v[i], sr, rr, fast_ok<FMT>(rowmax[i], rr), saturate);
+          if (rbase + i < rows) *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = b;
+        }
+      }
+      if (p.qt_scales != nullptr && col_ok && rchunk_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float sc = sh_col_s[cg * 8 + j], rc = sh_col_r[cg * 8 + j];
+          float cv[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
+          uint2 b = cast8<FMT>(cv, sc, rc, fast_ok<FMT>(Row8<InT>::colmax_bits(cmp, j), rc),
+                               saturate);
           *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = b;
         }
       }
@@ -703,6 +794,10 @@ cudaError_t dispatch_mode(const QuantParams &p, cudaStream_t stream) {
       return launch_variant<InT, FMT, kKDelayed>(p, stream);
     case kModeBlock:
       return launch_variant<InT, FMT, kKBlock>(p, stream);
+    case kModeRowAmax:
+      return launch_variant<InT, FMT, kKRowAmax>(p, stream);
+    case kModeRowCast:
+      return launch_variant<InT, FMT, kKRowCast>(p, stream);
     case kModeTile:
       if (p.q != nullptr && p.q_t != nullptr) return launch_variant<InT, FMT, kKTileBoth>(p, stream);
       if (p.q != nullptr) return launch_variant<InT, FMT, kKTileRow>(p, stream);
@@ -711,7 +806,20 @@ cudaError_t dispatch_mode(const QuantParams &p, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+// Row-wise pass 3: the amaxes left in a scale array become scales.
+__global__ void __launch_bounds__(256) amax_to_scale_kernel(float *s, int64_t n, float fm) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) s[i] = scale_from_amax(s[i], fm);
+}
+
 }  // namespace
+
+cudaError_t launch_amax_to_scale(float *s, int64_t n, int format, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const float fm = format == FP8Q_E4M3 ? 448.0f : 57344.0f;
+  amax_to_scale_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(s, n, fm);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream) {
   if (p.in_dtype == FP8Q_DT_BF16) {

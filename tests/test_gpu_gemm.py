@@ -357,3 +357,67 @@ def test_layer_dgrad_wgrad_full_size_delayed_vs_current(fq):
             ms, ns = _sample_points(Rr, Cc, rng, n=2048)
             yr, ab = oracle.gemm_points(opA, opB, ms, ns)
             check_bound(f32(got)[ms, ns], yr, ab, True, f"{mode} {nm}")
+
+
+# ------------------------------------------------------------- row scales
+
+@pytest.mark.parametrize("M,N,K", [(300, 272, 400), (1000, 1040, 1024), (64, 16, 16),
+                                   (257, 48, 2048)])
+@pytest.mark.parametrize("kinds", [("row", "row"), ("row", "tensor"), ("tensor", "row")])
+def test_row_scaled_shapes(fq, M, N, K, kinds):
+    a, _ = workloads.with_outlier_rows((M, K), 1.0, 0.05, 50.0, 80)
+    b = workloads.normal((N, K), 0.02, 81)
+    ad, bd = a.cuda(), b.cuda()
+    ops, rops = [], []
+    for kind, t, td, fmt in ((kinds[0], a, ad, 0), (kinds[1], b, bd, 1)):
+        if kind == "row":
+            q, s, _, _ = fq.fp8_quantize_rowwise(td, fmt)
+            rq, rs, _, _ = oracle.quantize_rowwise(to_oracle(t), fmt)
+            ops.append(fq.GemmOperand.row(q, fmt, s))
+            rops.append(oracle.GemmOperand.row(rq, fmt, rs))
+        else:
+            q, _, s = fq.fp8_quantize_tensor(td, fmt, fq.fp8_amax(td))
+            rq, _, rs = oracle.quantize_tensor(to_oracle(t), fmt)
+            ops.append(fq.GemmOperand.tensor(q, fmt, s))
+            rops.append(oracle.GemmOperand.tensor(rq, fmt, rs))
+        assert_bytes_equal(u8(q), rq, f"{kind} bytes")
+    y = fq.fp8_gemm(ops[0], ops[1], out_dtype=torch.bfloat16)
+    gpu_status_ok(fq)
+    yr, ab = oracle.gemm_rows(rops[0], rops[1])
+    check_bound(f32(y), yr, ab, True, f"{kinds} {M}x{N}x{K}")
+
+
+def test_rowwise_all_roles_full_size(fq):
+    """Attention-out layer at full size with row-wise scaling: Fprop (x rows,
+    w rows), Dgrad (g rows, columns of w), Wgrad (columns of g, columns of x)."""
+    idx = 1
+    shape = workloads.LAYER[idx]
+    x, w, g = workloads.layer_inputs(shape, idx)
+    M, K, N = x.shape[0], shape.K, shape.N
+    qx, sx, qxt, sxt = fq.fp8_quantize_rowwise(x.cuda(), 0, rows=True, cols=True)
+    qw, sw, qwt, swt = fq.fp8_quantize_rowwise(w.cuda(), 0, rows=True, cols=True)
+    qg, sg, qgt, sgt = fq.fp8_quantize_rowwise(g.cuda(), 1, rows=True, cols=True)
+    Rw = fq.GemmOperand.row
+    y = fq.fp8_gemm_fprop(Rw(qx, 0, sx), Rw(qw, 0, sw))
+    dx = fq.fp8_gemm_dgrad(Rw(qg, 1, sg), Rw(qwt, 0, swt))
+    dw = fq.fp8_gemm_wgrad(Rw(qgt, 1, sgt), Rw(qxt, 0, sxt))
+    gpu_status_ok(fq)
+    ref = {}
+    for nm, t, fmt, pair in (("x", x, 0, (qx, sx, qxt, sxt)), ("w", w, 0, (qw, sw, qwt, swt)),
+                             ("g", g, 1, (qg, sg, qgt, sgt))):
+        rq, rs, rqt, rst = oracle.quantize_rowwise(to_oracle(t), fmt, rows=True, cols=True)
+        assert_bytes_equal(u8(pair[0]), rq, nm)
+        assert_bytes_equal(u8(pair[2]), rqt, nm + "_t")
+        assert_f32_bits_equal(f32(pair[1]), rs, nm + " scales")
+        assert_f32_bits_equal(f32(pair[3]), rst, nm + "_t scales")
+        ref[nm] = (rq, rs, rqt, rst)
+    R = oracle.GemmOperand.row
+    rng = np.random.default_rng(5)
+    for got, opA, opB, Rr, Cc, nm in [
+        (y, R(ref["x"][0], 0, ref["x"][1]), R(ref["w"][0], 0, ref["w"][1]), M, N, "fprop"),
+        (dx, R(ref["g"][0], 1, ref["g"][1]), R(ref["w"][2], 0, ref["w"][3]), M, K, "dgrad"),
+        (dw, R(ref["g"][2], 1, ref["g"][3]), R(ref["x"][2], 0, ref["x"][3]), N, K, "wgrad"),
+    ]:
+        ms, ns = _sample_points(Rr, Cc, rng, n=2048)
+        yr, ab = oracle.gemm_points(opA, opB, ms, ns)
+        check_bound(f32(got)[ms, ns], yr, ab, True, nm)

@@ -244,3 +244,40 @@ def test_activation_tiles_full_size(fq, activation):
     mse_tile = np.mean((d_tile[keep] - xf[keep]) ** 2)
     mse_tensor = np.mean((d_tensor[keep] - xf[keep]) ** 2)
     assert mse_tile < mse_tensor
+
+
+# --------------------------------------------------------------- row-wise
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(128, 128), (200, 176), (16, 4096), (1024, 272), (272, 48)])
+@pytest.mark.parametrize("which", ["rows", "cols", "both"])
+def test_rowwise(fq, fmt, dtype, shape, which):
+    rows, cols = which in ("rows", "both"), which in ("cols", "both")
+    if cols and shape[0] % 16:
+        pytest.skip("column scales (transposed copy) need rows % 16 == 0")
+    x, _ = workloads.with_outlier_rows(shape, 0.5, 0.05, 300.0, 41, dtype=dtype)
+    x[: min(2, shape[0]), :].zero_()
+    x[:, : min(16, shape[1])] *= 20
+    q, qs, qt, qts = fq.fp8_quantize_rowwise(x.cuda(), fmt, rows=rows, cols=cols)
+    rq, rqs, rqt, rqts = oracle.quantize_rowwise(to_oracle(x), fmt, rows=rows, cols=cols)
+    if rows:
+        assert_f32_bits_equal(f32(qs), rqs, "row scales")
+        assert_bytes_equal(u8(q), rq, "row bytes")
+    if cols:
+        assert_f32_bits_equal(f32(qts), rqts, "column scales")
+        assert_bytes_equal(u8(qt), rqt, "column bytes")
+
+
+def test_rowwise_repeated_calls_reset_accumulators(fq):
+    """The scale arrays double as amax accumulators: a second call with
+    smaller data must not keep the first call's larger amaxes."""
+    x = workloads.normal((256, 512), 10.0, 42).cuda()
+    q, qs, qt, qts = fq.fp8_quantize_rowwise(x, 0, rows=True, cols=True)
+    y = (x * 1e-3).contiguous()
+    fq.fp8_quantize_rowwise(y, 0, rows=True, cols=True, q=q, q_scales=qs, q_t=qt, qt_scales=qts)
+    rq, rqs, rqt, rqts = oracle.quantize_rowwise(to_oracle(y.cpu()), 0, rows=True, cols=True)
+    assert_f32_bits_equal(f32(qs), rqs, "row scales")
+    assert_f32_bits_equal(f32(qts), rqts, "column scales")
+    assert_bytes_equal(u8(q), rq, "row bytes")
+    assert_bytes_equal(u8(qt), rqt, "column bytes")

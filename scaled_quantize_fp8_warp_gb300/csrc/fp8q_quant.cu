@@ -132,20 +132,24 @@ __device__ __forceinline__ uint32_t cast1_slow(float x, float s, int saturate) {
   return encode_slow<FMT>(v, saturate);
 }
 
+// Out of line, with the eight values as scalars: they travel in registers,
+// so a caller's fast path keeps no copy of them in local memory.
 template <int FMT>
-__device__ __noinline__ uint2 cast8_slow(const float (&v)[8], float s, int saturate) {
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) b[j] = cast1_slow<FMT>(v[j], s, saturate);
-  return make_uint2(b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24),
-                    b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24));
+__device__ __noinline__ uint2 cast8_slow(float v0, float v1, float v2, float v3, float v4,
+                                         float v5, float v6, float v7, float s, int saturate) {
+  const uint32_t b0 = cast1_slow<FMT>(v0, s, saturate), b1 = cast1_slow<FMT>(v1, s, saturate);
+  const uint32_t b2 = cast1_slow<FMT>(v2, s, saturate), b3 = cast1_slow<FMT>(v3, s, saturate);
+  const uint32_t b4 = cast1_slow<FMT>(v4, s, saturate), b5 = cast1_slow<FMT>(v5, s, saturate);
+  const uint32_t b6 = cast1_slow<FMT>(v6, s, saturate), b7 = cast1_slow<FMT>(v7, s, saturate);
+  return make_uint2(b0 | (b1 << 8) | (b2 << 16) | (b3 << 24),
+                    b4 | (b5 << 8) | (b6 << 16) | (b7 << 24));
 }
 
 template <int FMT>
 __device__ __forceinline__ uint2 cast8(const float (&v)[8], float s, float r, bool fast,
                                        int saturate) {
   if (fast) return cast8_fast<FMT>(v, s, r);
-  return cast8_slow<FMT>(v, s, saturate);
+  return cast8_slow<FMT>(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], s, saturate);
 }
 
 // Quotients of every value with |x| <= m stay on the fast path's domain.
@@ -267,10 +271,8 @@ template <int FMT, typename InT>
 __device__ __forceinline__ uint2 cast_row(const Row8<InT> &x, float s, float r, bool fast,
                                           int saturate) {
   if (fast) return cast_row_fast<FMT>(x, s, r);
-  float v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) v[j] = x.at(j);
-  return cast8_slow<FMT>(v, s, saturate);
+  return cast8_slow<FMT>(x.at(0), x.at(1), x.at(2), x.at(3), x.at(4), x.at(5), x.at(6),
+                         x.at(7), s, saturate);
 }
 
 // 4x4 byte transpose: a..d are rows (byte k = column k); o0..o3 are columns.

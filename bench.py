@@ -44,7 +44,7 @@ L2_BYTES = 126 * 1024 * 1024
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[1])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["fp8q", "reference"], default="fp8q")
     ap.add_argument("--no-cpu-baseline", action="store_true",
@@ -61,9 +61,12 @@ PROFILE_CASES = {
     "gemm_tensor": "8192x8192x8192 per-tensor E4M3 GEMM, bf16 out",
     "gemm_block": "8192x8192x8192 1x128 x 128x128 GEMM, bf16 out",
     "gemm_tile": "8192x8192x8192 1x128 x 1x128 GEMM (wgrad form), bf16 out",
+    "gemm_row": "8192x8192x8192 row-scaled x row-scaled E4M3 GEMM, bf16 out",
     "quant_tile_dual": "16384x8192 bf16, 1x128 row and column tiles, E4M3",
     "quant_tile_rows": "16384x8192 bf16, 1x128 row tiles, E4M3",
     "quant_block": "16384x8192 bf16, 128x128 blocks + transposed copy, E4M3",
+    "quant_rowwise": "16384x8192 bf16, row-wise scales, q and the transposed copy, E4M3",
+    "quant_tensor_dual": "16384x8192 bf16, per-tensor scale, q and the transposed copy, E4M3",
     "amax": "16384x8192 bf16 amax",
     "quant_activation": ("the bench's 8192x4096 activation, 1x128 row tiles, E4M3, L2 flushed "
                          "before each of the three calls"),
@@ -85,6 +88,10 @@ def run_profile_case(case: str):
             qa, _, sa = fq.fp8_quantize_tensor(a, fq.E4M3, fq.fp8_amax(a))
             qb, _, sb = fq.fp8_quantize_tensor(b, fq.E4M3, fq.fp8_amax(b))
             A, B = fq.GemmOperand.tensor(qa, 0, sa), fq.GemmOperand.tensor(qb, 0, sb)
+        elif case == "gemm_row":
+            qa, sa, _, _ = fq.fp8_quantize_rowwise(a, fq.E4M3)
+            qb, sb, _, _ = fq.fp8_quantize_rowwise(b, fq.E4M3)
+            A, B = fq.GemmOperand.row(qa, 0, sa), fq.GemmOperand.row(qb, 0, sb)
         else:
             qa, sa, _, _ = fq.fp8_quantize_tile1x128(a, fq.E4M3)
             A = fq.GemmOperand.tile(qa, 0, sa)
@@ -112,6 +119,10 @@ def run_profile_case(case: str):
                 fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True, cols=True)
             elif case == "quant_tile_rows":
                 fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True)
+            elif case == "quant_tensor_dual":
+                fq.fp8_quantize_tensor(x, fq.E4M3, fq.fp8_amax(x), want_q=True, want_qt=True)
+            elif case == "quant_rowwise":
+                fq.fp8_quantize_rowwise(x, fq.E4M3, rows=True, cols=True)
             elif case == "quant_block":
                 fq.fp8_quantize_block128x128(x, fq.E4M3, want_q=True, want_qt=True)
             else:
@@ -188,22 +199,28 @@ class Dist:
 # -------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Samples nvidia-smi for this process's GPU during the timed region."""
+    """Samples nvidia-smi for this process's GPU every 50 ms while the layer
+    phases run; time_steps() records the wall-clock window of each timed
+    region, and the summary keeps only the samples whose own nvidia-smi
+    timestamp falls inside one of those windows."""
 
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
         self.lines = []
+        self.windows = []   # (t0, t1) wall-clock seconds of the timed regions
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except (OSError, FileNotFoundError):
@@ -216,7 +233,7 @@ class ClockSampler:
 
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(2 * self.PERIOD_MS / 1000)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -224,26 +241,44 @@ class ClockSampler:
                 self.proc.kill()
             self.reader.join(timeout=2)
 
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        rows = []
+        rows, in_window = [], []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
-            if self.uuid and parts[0] != self.uuid:
+            if self.uuid and parts[1] != self.uuid:
                 continue
-            rows.append(parts)
+            rows.append(parts[1:])
+            t = self._epoch(parts[0])
+            if t is not None and any(a <= t <= b for a, b in self.windows):
+                in_window.append(parts[1:])
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        use = in_window if in_window else rows
+        num = lambda v: v.replace(".", "").isdigit()
+        sm = [float(r[1]) for r in use if num(r[1])]
+        smax = [float(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i] == "Active"})
+        power = [float(r[3]) for r in use if num(r[3])]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows),
-                "power_w_max": max(power) if power else None}
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_regions": len(in_window),
+                "power_w_median": statistics.median(power) if power else None,
+                "power_w_max": max(power) if power else None,
+                "period_ms": self.PERIOD_MS,
+                "span": "the timed regions of the layer phases (per-tensor, delayed, "
+                        "block-scaled, row-wise)"}
 
 
 # ------------------------------------------------------------- layer buffers
@@ -277,6 +312,10 @@ class LayerState:
             L["sx"], L["sxt"] = e(((K + 127) // 128, M), f32), e(((M + 127) // 128, K), f32)
             L["sw"] = e(((N + 127) // 128, (K + 127) // 128), f32)
             L["sg"], L["sgt"] = e(((N + 127) // 128, M), f32), e(((M + 127) // 128, N), f32)
+            # row-wise recipe: one scale per row of each K-major operand
+            L["rx"], L["rxt"] = e((M,), f32), e((K,), f32)
+            L["rw"], L["rwt"] = e((N,), f32), e((K,), f32)
+            L["rg"], L["rgt"] = e((M,), f32), e((N,), f32)
             # per-tensor recipe scalars
             for nm in ("ax", "aw", "ag", "tx", "tw", "tg"):
                 L[nm] = e((1,), f32)
@@ -323,6 +362,20 @@ class LayerState:
         return ops
 
 
+    def row_operands(self):
+        fq = self.fq
+        R = fq.GemmOperand.row
+        ops = []
+        for L in self.linears:
+            ops.append({
+                "fprop": (R(L["qx"], fq.E4M3, L["rx"]), R(L["qw"], fq.E4M3, L["rw"]), L["y"]),
+                "dgrad": (R(L["qg"], fq.E5M2, L["rg"]), R(L["qwt"], fq.E4M3, L["rwt"]), L["dx"]),
+                "wgrad": (R(L["qgt"], fq.E5M2, L["rgt"]), R(L["qxt"], fq.E4M3, L["rxt"]),
+                          L["dw"]),
+            })
+        return ops
+
+
 class Runner:
     """Issues the steps; optionally brackets each GEMM with CUDA events."""
 
@@ -331,6 +384,7 @@ class Runner:
         self.fq, self.torch = state.fq, state.torch
         self.bops = state.block_operands()
         self.tops = state.tensor_operands()
+        self.rops = state.row_operands()
         self.gemm_events = None   # list of (start, end, flops) when recording
 
     def _gemm(self, role, A, B, C):
@@ -415,6 +469,22 @@ class Runner:
     def tensor_prequant(self):
         self.gemms(self.tops)
 
+    # row-wise recipe ----------------------------------------------------
+    def row_autocast(self):
+        fq, st = self.fq, self.stream
+        for L, o in zip(self.s.linears, self.rops):
+            for nm, fmt in (("x", fq.E4M3), ("w", fq.E4M3), ("g", fq.E5M2)):
+                fq.fp8_quantize_rowwise(L[nm], fmt, rows=True, cols=True, q=L["q" + nm],
+                                        q_scales=L["r" + nm], q_t=L["q" + nm + "t"],
+                                        qt_scales=L["r" + nm + "t"], stream=st)
+            for role in ("fprop", "dgrad", "wgrad"):
+                self._gemm(role, *o[role])
+
+    row_autocast.launches = 4 * 15   # per linear: 3 x (2 quantize passes + 2 finalizes), 3 GEMMs
+
+    def row_prequant(self):
+        self.gemms(self.rops)
+
     # end to end: host inputs in, host outputs out --------------------------
     def e2e_tensor(self):
         """One step with the inputs copied in from pinned host memory and the
@@ -478,7 +548,7 @@ class Runner:
                 L["dw_h"].copy_(L["dw"], non_blocking=True)
 
 
-def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None):
+def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None, clk=None):
     """W untimed steps, then exactly K timed steps between barriers and
     device synchronisations; returns the max-over-ranks ms per step."""
     for _ in range(warmup):
@@ -486,6 +556,7 @@ def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None):
     torch.cuda.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
+    t_start = time.time()
     if flush is None:
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -509,6 +580,8 @@ def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None):
             e1.record(stream)
             torch.cuda.synchronize()
             ms += e0.elapsed_time(e1)
+    if clk is not None:
+        clk.windows.append((t_start, time.time()))
     dist.barrier()
     torch.cuda.synchronize()
     return dist.max(ms / steps)
@@ -674,20 +747,29 @@ def main():
         fl = sum(f for _, _, f in events)
         return ms, fl, len(events)
 
-    # ---- headline: the layer with per-tensor current scaling, autocast
+    # ---- headline: the layer with per-tensor current scaling, autocast;
+    # clocks are sampled through every timed layer phase
     with ClockSampler(uuid) as clk:
         ms_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(False), K, W,
-                             record=run)
-    t_gemm_ms, t_gemm_fl, t_gemm_n = gemm_summary(run.gemm_events)
-    run.gemm_events = None
-    ms_pre = time_steps(torch, dist, stream, run.tensor_prequant, K, W)
-    ms_d_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(True), K, W)
+                             record=run, clk=clk)
+        t_gemm_ms, t_gemm_fl, t_gemm_n = gemm_summary(run.gemm_events)
+        run.gemm_events = None
+        ms_pre = time_steps(torch, dist, stream, run.tensor_prequant, K, W, clk=clk)
+        ms_d_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(True), K, W,
+                               clk=clk)
 
-    # ---- the same layer with 1x128 / 128x128 scaling
-    ms_b_auto = time_steps(torch, dist, stream, run.block_autocast, K, W, record=run)
-    b_gemm_ms, b_gemm_fl, b_gemm_n = gemm_summary(run.gemm_events)
-    run.gemm_events = None
-    ms_b_pre = time_steps(torch, dist, stream, run.block_prequant, K, W)
+        # ---- the same layer with 1x128 / 128x128 scaling
+        ms_b_auto = time_steps(torch, dist, stream, run.block_autocast, K, W, record=run,
+                               clk=clk)
+        b_gemm_ms, b_gemm_fl, b_gemm_n = gemm_summary(run.gemm_events)
+        run.gemm_events = None
+        ms_b_pre = time_steps(torch, dist, stream, run.block_prequant, K, W, clk=clk)
+
+        # ---- the same layer with row-wise scaling
+        ms_r_auto = time_steps(torch, dist, stream, run.row_autocast, K, W, record=run, clk=clk)
+        r_gemm_ms, r_gemm_fl, r_gemm_n = gemm_summary(run.gemm_events)
+        run.gemm_events = None
+        ms_r_pre = time_steps(torch, dist, stream, run.row_prequant, K, W, clk=clk)
 
     # ---- end to end through host buffers (headline recipe)
     ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), 1)
@@ -726,6 +808,22 @@ def main():
         fq.fp8_quantize_tensor(xq, fq.E4M3, am, q=qt, scale=sc, stream=stream)), QK, W,
         flush=flush)
     tile_bytes = n * 2 + n * 1 + 4 * n // 128
+    # both orientations (q and the transposed copy q_t), as the layer uses them
+    qtt = torch.empty((C, R), dtype=torch.uint8, device=xq.device)
+    stt = torch.empty(((R + 127) // 128, C), dtype=torch.float32, device=xq.device)
+    rs_r = torch.empty((R,), dtype=torch.float32, device=xq.device)
+    rs_c = torch.empty((C,), dtype=torch.float32, device=xq.device)
+    ms_tile2 = time_steps(torch, dist, stream, lambda: fq.fp8_quantize_tile1x128(
+        xq, fq.E4M3, rows=True, cols=True, q=qt, q_scales=st, q_t=qtt, qt_scales=stt,
+        stream=stream), QK, W, flush=flush)
+    ms_row2 = time_steps(torch, dist, stream, lambda: fq.fp8_quantize_rowwise(
+        xq, fq.E4M3, rows=True, cols=True, q=qt, q_scales=rs_r, q_t=qtt, qt_scales=rs_c,
+        stream=stream), QK, W, flush=flush)
+    ms_tensor2 = time_steps(torch, dist, stream, lambda: (
+        fq.fp8_amax(xq, out=am, stream=stream),
+        fq.fp8_quantize_tensor(xq, fq.E4M3, am, want_q=True, want_qt=True, q=qt, q_t=qtt,
+                               scale=sc, stream=stream)), QK, W, flush=flush)
+    dual_bytes = n * 2 + 2 * n     # read x once, write q and q_t (scales are < 0.1%)
     gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
 
     # ---- CPU baseline (oracle on the host cores, rank 0, N = 1 only)
@@ -747,6 +845,7 @@ def main():
     fp8_peak_burst = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     t_gemm_tflops = t_gemm_fl / (t_gemm_ms * 1e-3) / 1e12
     b_gemm_tflops = b_gemm_fl / (b_gemm_ms * 1e-3) / 1e12
+    r_gemm_tflops = r_gemm_fl / (r_gemm_ms * 1e-3) / 1e12
     tile_gbps = gbps(tile_bytes, ms_tile)
     tf = lambda ms: flops / (ms * 1e-3) / 1e12
     peak_src = (f"{peak_src}: bf16_tflops_sustained x {FP8_PER_BF16} (dense FP8/BF16 nominal "
@@ -782,6 +881,15 @@ def main():
                          "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_blockscaled_kernel"),
                          "kernel": "gemm_blockscaled_kernel",
                          "launches": b_gemm_n}},
+        "rowwise": {
+            "workload": ("the same 12 GEMMs with one scale per row of each K-major operand "
+                         "(x, w and grad_out quantised along both orientations)"),
+            "autocast": {"value": tf(ms_r_auto), "ms_per_step": ms_r_auto},
+            "prequant": {"value": tf(ms_r_pre), "ms_per_step": ms_r_pre},
+            "unit": "TFLOP/s",
+            "gemm": {"achieved": r_gemm_tflops, "frac": r_gemm_tflops / fp8_peak_sust,
+                     "kernel": "gemm_tensor_kernel, vector-scale epilogue",
+                     "launches": r_gemm_n}},
         "context_pages_B300_ms_per_layer": {
             "fp8_current_autocast": 9.15, "fp8_current_prequant": 6.81,
             "fp8_delayed_autocast": 7.80, "mxfp8_autocast": 8.98,
@@ -796,6 +904,17 @@ def main():
             "tensor_current": {"GB/s (over 3 B/elem)": gbps(3 * n, ms_tensor),
                                "us": ms_tensor * 1e3,
                                "frac": gbps(3 * n, ms_tensor) / hbm_peak},
+            "both_orientations": {
+                "note": ("q and q_t from one call; GB/s over the unique bytes (2 B read + "
+                         "2 B written per element); row-wise and per-tensor read x twice "
+                         "(amax pass, then cast), the second read mostly from L2"),
+                "tile1x128_rows_and_cols": {"GB/s": gbps(dual_bytes, ms_tile2),
+                                            "us": ms_tile2 * 1e3,
+                                            "frac": gbps(dual_bytes, ms_tile2) / hbm_peak},
+                "rowwise": {"GB/s": gbps(dual_bytes, ms_row2), "us": ms_row2 * 1e3,
+                            "frac": gbps(dual_bytes, ms_row2) / hbm_peak},
+                "tensor_current": {"GB/s": gbps(dual_bytes, ms_tensor2), "us": ms_tensor2 * 1e3,
+                                   "frac": gbps(dual_bytes, ms_tensor2) / hbm_peak}},
             "unit": "GB/s", "peak": hbm_peak,
         },
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,

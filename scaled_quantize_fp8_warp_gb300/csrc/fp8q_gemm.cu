@@ -49,8 +49,15 @@ constexpr int kGroupM = 16;         // M-tiles per raster group
 #ifndef FP8Q_TENSOR_BK
 #define FP8Q_TENSOR_BK 128
 #endif
+#ifndef FP8Q_TENSOR_CM
+#define FP8Q_TENSOR_CM 2
+#endif
 // K-block width of the per-tensor kernel at BN = 256 (64 -> a deeper ring).
 constexpr int kTensorBK = FP8Q_TENSOR_BK;
+// CTAs per cluster of the per-tensor kernel at BN = 256 (1, 2 or 4): they
+// share B's tile through TMA multicast.
+constexpr int kTensorCM = FP8Q_TENSOR_CM;
+static_assert(kTensorCM == 1 || kTensorCM == 2 || kTensorCM == 4, "cluster of 1, 2 or 4");
 constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
 constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 
@@ -69,11 +76,12 @@ struct GemmArgs {
   unsigned int *err;
 };
 
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mt, int &nt) {
-  const int per_group = kGroupM * num_n;
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mt, int &nt,
+                                            int group_m = kGroupM) {
+  const int per_group = group_m * num_n;
   const int g = tile / per_group;
-  const int first_m = g * kGroupM;
-  const int gsize = min(num_m - first_m, kGroupM);
+  const int first_m = g * group_m;
+  const int gsize = min(num_m - first_m, group_m);
   const int local = tile - g * per_group;
   mt = first_m + local % gsize;
   nt = local / gsize;
@@ -107,18 +115,27 @@ struct Layout {
   static constexpr int kSmemBytes = kRingBytes + kBarBytes + 16 + 1024;  // + align slack
 };
 
-// Producer loop shared by both kernels.
-template <int BN, int STAGES, int BK = kBK>
+// Producer loop shared by both kernels.  With CM > 1 the CTAs of a cluster
+// work on the CM vertically adjacent tiles (CM u + r, n) of unit u at the same
+// time; they share B's tile, each loading BN / CM of its rows with multicast
+// into every CTA's ring slot, so a slot is refilled only once every CTA's
+// MMAs have released it (its empty barrier counts CM arrivals).
+template <int BN, int STAGES, int BK = kBK, int CM = 1>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUtensorMap *tb,
                                               const GemmArgs &p, uint32_t ring, uint32_t bars,
-                                              volatile int *abort_flag) {
+                                              volatile int *abort_flag, uint32_t rank = 0) {
   using L = Layout<BN, STAGES, BK>;
-  const int total = p.num_m_tiles * p.num_n_tiles;
+  constexpr int kPartRows = BN / CM;
+  const int num_mu = (p.num_m_tiles + CM - 1) / CM;
+  const int total = num_mu * p.num_n_tiles;
   uint32_t it = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-    int mt, nt;
-    tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
+  for (int u = blockIdx.x / CM; u < total && ok; u += gridDim.x / CM) {
+    int mu, nt;
+    tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / CM);
+    // a CTA past the last M tile (odd tile count) re-reads that tile's A rows
+    // and stores nothing: it still has to deliver its part of B
+    const int mt = min(mu * CM + (int)rank, p.num_m_tiles - 1);
     for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
       const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
       const uint32_t full = bars + 8 * s, empty = bars + 8 * (STAGES + s);
@@ -129,7 +146,22 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUten
       const uint32_t sa = ring + s * L::kStageBytes;
       mbar_arrive_expect_tx(full, L::kStageBytes);
       tma_load_2d(sa, ta, kb * BK, mt * kBM, full);
-      tma_load_2d(sa + L::kABytes, tb, kb * BK, nt * BN, full);
+      if (CM == 1)
+        tma_load_2d(sa + L::kABytes, tb, kb * BK, nt * BN, full);
+      else
+        tma_load_2d_multicast(sa + L::kABytes + rank * (kPartRows * BK), tb, kb * BK,
+                              nt * BN + (int)rank * kPartRows, full, (uint16_t)((1u << CM) - 1));
+    }
+  }
+  if (ok && CM > 1) {
+    // Wait until every CTA has released every slot for the last time: after
+    // this no arrival from another CTA is still on its way to this CTA.
+    for (uint32_t j = 0, jt = it; j < (uint32_t)STAGES; ++j, ++jt) {
+      if (!wait_bounded(bars + 8 * (STAGES + jt % STAGES), ((jt / STAGES) & 1u) ^ 1u,
+                        abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
     }
   }
   if (!ok) {
@@ -203,7 +235,7 @@ __device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n
 // ------------------------------------------------------------------------
 // Per-tensor scaled GEMM: 6 warps (producer, MMA, 4 epilogue warps).
 // ------------------------------------------------------------------------
-template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC>
+template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC, int CM>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap ta,
                        const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
@@ -221,10 +253,12 @@ __global__ void __launch_bounds__(192, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
+  constexpr uint16_t kAllCtas = (uint16_t)((1u << CM) - 1);
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CM);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -243,18 +277,21 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
-  const int total = p.num_m_tiles * p.num_n_tiles;
+  const int num_mu = (p.num_m_tiles + CM - 1) / CM;
+  const int total = num_mu * p.num_n_tiles;
+  const int unit0 = blockIdx.x / CM, unit_step = gridDim.x / CM;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<BN, STAGES, BK>(&ta, &tb, p, ring, bars, abort_flag);
+    if (lane == 0) producer_loop<BN, STAGES, BK, CM>(&ta, &tb, p, ring, bars, abort_flag, rank);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++acc_it) {
+      for (int u = unit0; u < total && ok; u += unit_step, ++acc_it) {
         const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
         if (!wait_bounded(acce0 + 8 * buf, aph ^ 1u, abort_flag, p.err)) {
           ok = false;
@@ -270,7 +307,10 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after();
           issue_kblock<BN, STAGES, BK>(ring, s, d_tmem, p.idesc, kb > 0);
-          mma_commit(empty0 + 8 * s);
+          if (CM == 1)
+            mma_commit(empty0 + 8 * s);
+          else
+            mma_commit_multicast(empty0 + 8 * s, kAllCtas);
         }
         if (!ok) break;
         mma_commit(accf0 + 8 * buf);
@@ -285,9 +325,10 @@ __global__ void __launch_bounds__(192, 1)
     // thread's row times s_B of each column, applied the same way.
     const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
     uint32_t acc_it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++acc_it) {
-      int mt, nt;
-      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt);
+    for (int u = unit0; u < total; u += unit_step, ++acc_it) {
+      int mu, nt;
+      tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / CM);
+      const int mt = mu * CM + (int)rank;   // >= num_m_tiles: nothing to store
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
       if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
       tc_fence_after();
@@ -323,6 +364,7 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) cluster_sync_all();  // no CTA leaves while another may still signal it
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -571,17 +613,44 @@ cudaError_t set_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC>
+template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC, int CM>
 int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                cudaStream_t stream) {
   using L = Layout<BN, STAGES, BK>;
-  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16, VEC>;
+  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16, VEC, CM>;
   static bool attr_done = false;  // per instantiation
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  if (CM > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   if (!attr_done) {
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (CM > 1) {
+      // clusters that can be resident at once: a persistent grid larger than
+      // that would leave clusters waiting for others to finish
+      cfg.gridDim = dim3(CM * (sm_count() / CM), 1, 1);
+      if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
+          max_clusters < 1)
+        return FP8Q_ERR_CUDA;
+    }
     attr_done = true;
   }
-  kernel<<<grid, 192, L::kSmemBytes, stream>>>(ta, tb, a);
+  if (CM > 1) {
+    const int units = ((a.num_m_tiles + CM - 1) / CM) * a.num_n_tiles;
+    grid = CM * (units < max_clusters ? units : max_clusters);
+  }
+  cfg.gridDim = dim3(grid, 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, a) != cudaSuccess) return FP8Q_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
@@ -661,9 +730,12 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   // Per-tensor scaling is free to pick its K-block width; tile/block scaling
   // needs the 128-wide K blocks its scales are defined on.
   const int BK = (tensor && BN == 256) ? kTensorBK : kBK;
+  // The 256-wide per-tensor kernel runs in clusters of kTensorCM CTAs that
+  // each load BN / kTensorCM rows of B's tile.
+  const int b_box_rows = (tensor && BN == 256) ? BN / kTensorCM : BN;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, (uint32_t)BK, kBM) ||
-      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)BK, (uint32_t)BN))
+      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)BK, (uint32_t)b_box_rows))
     return FP8Q_ERR_CUDA;
 
   GemmArgs a{};
@@ -694,22 +766,22 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
     constexpr int S256 = kTensorBK == 64 ? 9 : 4;   // ~216 KB or ~192 KB of ring
     if (vec) {
       if (BN == 64)
-        return bf16 ? run_tensor<64, 8, 128, true, true>(ta, tb, a, grid, stream)
-                    : run_tensor<64, 8, 128, false, true>(ta, tb, a, grid, stream);
+        return bf16 ? run_tensor<64, 8, 128, true, true, 1>(ta, tb, a, grid, stream)
+                    : run_tensor<64, 8, 128, false, true, 1>(ta, tb, a, grid, stream);
       if (BN == 128)
-        return bf16 ? run_tensor<128, 6, 128, true, true>(ta, tb, a, grid, stream)
-                    : run_tensor<128, 6, 128, false, true>(ta, tb, a, grid, stream);
-      return bf16 ? run_tensor<256, S256, kTensorBK, true, true>(ta, tb, a, grid, stream)
-                  : run_tensor<256, S256, kTensorBK, false, true>(ta, tb, a, grid, stream);
+        return bf16 ? run_tensor<128, 6, 128, true, true, 1>(ta, tb, a, grid, stream)
+                    : run_tensor<128, 6, 128, false, true, 1>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<256, S256, kTensorBK, true, true, kTensorCM>(ta, tb, a, grid, stream)
+                  : run_tensor<256, S256, kTensorBK, false, true, kTensorCM>(ta, tb, a, grid, stream);
     }
     if (BN == 64)
-      return bf16 ? run_tensor<64, 8, 128, true, false>(ta, tb, a, grid, stream)
-                  : run_tensor<64, 8, 128, false, false>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<64, 8, 128, true, false, 1>(ta, tb, a, grid, stream)
+                  : run_tensor<64, 8, 128, false, false, 1>(ta, tb, a, grid, stream);
     if (BN == 128)
-      return bf16 ? run_tensor<128, 6, 128, true, false>(ta, tb, a, grid, stream)
-                  : run_tensor<128, 6, 128, false, false>(ta, tb, a, grid, stream);
-    return bf16 ? run_tensor<256, S256, kTensorBK, true, false>(ta, tb, a, grid, stream)
-                : run_tensor<256, S256, kTensorBK, false, false>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<128, 6, 128, true, false, 1>(ta, tb, a, grid, stream)
+                  : run_tensor<128, 6, 128, false, false, 1>(ta, tb, a, grid, stream);
+    return bf16 ? run_tensor<256, S256, kTensorBK, true, false, kTensorCM>(ta, tb, a, grid, stream)
+                : run_tensor<256, S256, kTensorBK, false, false, kTensorCM>(ta, tb, a, grid, stream);
   }
   const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
   constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;

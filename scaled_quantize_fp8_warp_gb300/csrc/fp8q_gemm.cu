@@ -58,6 +58,17 @@ constexpr int kTensorBK = FP8Q_TENSOR_BK;
 // share B's tile through TMA multicast.
 constexpr int kTensorCM = FP8Q_TENSOR_CM;
 static_assert(kTensorCM == 1 || kTensorCM == 2 || kTensorCM == 4, "cluster of 1, 2 or 4");
+#ifndef FP8Q_TENSOR_PAIR
+#define FP8Q_TENSOR_PAIR 1
+#endif
+#ifndef FP8Q_PAIR_ACC
+#define FP8Q_PAIR_ACC 2
+#endif
+// Per-tensor / row scaling at N > 128 on CTA pairs (cta_group::2) with
+// kPairAcc TMEM accumulators of 256 columns each.
+constexpr bool kTensorPair = FP8Q_TENSOR_PAIR != 0;
+constexpr int kPairAcc = FP8Q_PAIR_ACC;
+constexpr int kPairStages = 6;
 constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
 constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 
@@ -370,6 +381,214 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ------------------------------------------------------------------------
+// Per-tensor (or row) scaled GEMM on CTA pairs: tcgen05.mma.cta_group::2.
+// A cluster of two CTAs computes one 256 x 256 tile.  Each CTA stages its
+// own 128 rows of A and its own 128 of the tile's 256 B rows per K block
+// (32 KB a stage instead of 48 KB for a 128 x 256 tile on one SM, so six
+// stages fit where four did); the even CTA's MMA thread issues M = 256,
+// N = 256 MMAs that read both CTAs' shared memory and write rows 0-127 of D
+// into its own TMEM and rows 128-255 into the peer's.  Both CTAs' loads
+// count on the even CTA's full barriers; its commits release the slots of
+// both CTAs and hand each CTA's epilogue its half of D; both epilogues
+// release the accumulator on the even CTA's barrier (8 warps).
+// ------------------------------------------------------------------------
+template <int STAGES>
+struct PairLayout {
+  static constexpr int kABytes = kBM * kBK;        // this CTA's 128 rows of A
+  static constexpr int kBBytes = 128 * kBK;        // this CTA's 128 rows of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kRingBytes = STAGES * kStageBytes;
+  static constexpr int kBarBytes = 8 * (2 * STAGES + 5);
+  static constexpr int kSmemBytes = kRingBytes + kBarBytes + 16 + 1024;
+};
+
+template <int STAGES, int ACC, bool OUT_BF16, bool VEC>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap ta,
+                            const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
+  constexpr int BN = 256;
+  using L = PairLayout<STAGES>;
+  constexpr uint32_t kTmemCols = ACC * BN;
+  constexpr uint16_t kBoth = 3;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t bars = ring + L::kRingBytes;
+  const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
+  const uint32_t accf0 = bars + 8 * (2 * STAGES), acce0 = accf0 + 16;
+  const uint32_t drain = acce0 + 16;
+  const uint32_t slot = bars + L::kBarBytes;
+  uint8_t *slot_ptr = smem_raw + (slot - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0: issues the pair's MMAs
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 8);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    prefetch_tmap(&ta);
+    prefetch_tmap(&tb);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
+  // One allocation serves the pair: both CTAs must hold the same address.
+  // Otherwise neither does any work (a symmetric decision, no waiting).
+  const bool paired = ld_shared_cluster_u32(mapa_shared(slot, rank ^ 1u)) == tmem_base;
+  if (!paired && threadIdx.x == 0) atomicOr(p.err, 4u);
+
+  const int num_mu = (p.num_m_tiles + 1) / 2;
+  const int total = num_mu * p.num_n_tiles;
+  const int unit0 = blockIdx.x / 2, unit_step = gridDim.x / 2;
+
+  if (!paired) {
+  } else if (warp == 0) {
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = unit0; u < total && ok; u += unit_step) {
+        int mu, nt;
+        tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / 2);
+        // past the last M tile (odd count): re-read that tile's A, store nothing
+        const int mt = min(2 * mu + (int)rank, p.num_m_tiles - 1);
+        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = ring + s * L::kStageBytes;
+          const uint32_t full_even = mapa_shared(full0 + 8 * s, 0);
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * L::kStageBytes);
+          tma_load_2d_pair(sa, &ta, kb * kBK, mt * kBM, full_even);
+          tma_load_2d_pair(sa + L::kABytes, &tb, kb * kBK, nt * BN + (int)rank * 128, full_even);
+        }
+      }
+      // every slot's last release (the even CTA's commits) has arrived here
+      for (uint32_t j = 0, jt = it; ok && j < (uint32_t)STAGES; ++j, ++jt)
+        ok = wait_bounded(empty0 + 8 * (jt % STAGES), ((jt / STAGES) & 1u) ^ 1u, abort_flag,
+                          p.err);
+      if (!ok) {
+        // aborting: give copies already issued (their barrier may be the
+        // other CTA's) a millisecond to land before the CTA can leave
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int u = unit0; u < total && ok; u += unit_step, ++acc_it) {
+        const uint32_t buf = ACC == 2 ? (acc_it & 1u) : 0u;
+        const uint32_t aph = ACC == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+        if (!wait_bounded(acce0 + 8 * buf, aph ^ 1u, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * BN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+          if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = ring + s * L::kStageBytes, b0 = a0 + L::kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = sdesc_k(a0 + k * kUmmaK, Swz<kBK>::kSBO, Swz<kBK>::kMode);
+            const uint64_t bd = sdesc_k(b0 + k * kUmmaK, Swz<kBK>::kSBO, Swz<kBK>::kMode);
+            mma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit_pair_multicast(empty0 + 8 * s, kBoth);
+        }
+        if (!ok) break;
+        mma_commit_pair_multicast(accf0 + 8 * buf, kBoth);
+      }
+      mma_commit_pair(drain);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0) && globaltimer_ns() - t0 < 200000000ull) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // Epilogue warps 2..5 -> TMEM lane quarters 2, 3, 0, 1 of this CTA's
+    // 128 rows of the pair tile.
+    const int quarter = warp & 3;
+    const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
+    const uint32_t acce_even0 = mapa_shared(acce0, 0);
+    uint32_t acc_it = 0;
+    for (int u = unit0; u < total; u += unit_step, ++acc_it) {
+      int mu, nt;
+      tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / 2);
+      const int mt = 2 * mu + (int)rank;   // >= num_m_tiles: nothing to store
+      const uint32_t buf = ACC == 2 ? (acc_it & 1u) : 0u;
+      const uint32_t aph = ACC == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+      if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
+      float sa = 0.0f;
+      if (VEC)
+        sa = p.a_row ? (m < p.M ? p.scale_a[m * p.a_stride_row] : 0.0f) : p.scale_a[0];
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * BN + c * 32, r);
+        tmem_ld_wait();
+        float v[32];
+        const int64_t n0 = (int64_t)nt * BN + c * 32;
+        if (VEC) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float sb = p.b_row ? (n0 + j < p.N ? p.scale_b[(n0 + j) * p.b_stride_row] : 0.0f)
+                                     : p.scale_b[0];
+            v[j] = __fmul_rn(__uint_as_float(r[j]), __fmul_rn(sa, sb));
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
+        }
+        if (m < p.M && n0 < p.N) store32<OUT_BF16>(p.C, p.N, m, n0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(acce0 + 8 * buf);
+        else
+          mbar_arrive_cluster(acce_even0 + 8 * buf);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the other may still signal it
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+// ------------------------------------------------------------------------
 // Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0) and the MMA
 // issuer (warp 1); NWG promotion warpgroups follow, warpgroup g owning tile
 // columns [g C, g C + C) with C = BN / NWG.  A carries 1x128 tile scales; B
@@ -613,6 +832,40 @@ cudaError_t set_smem(KernelT kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+template <int STAGES, int ACC, bool OUT_BF16, bool VEC>
+int run_tensor_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
+                    cudaStream_t stream) {
+  using L = PairLayout<STAGES>;
+  auto kernel = gemm_tensor_pair_kernel<STAGES, ACC, OUT_BF16, VEC>;
+  static bool attr_done = false;  // per instantiation
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!attr_done) {
+    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
+        max_clusters < 1)
+      return FP8Q_ERR_CUDA;
+    attr_done = true;
+  }
+  GemmArgs pa = a;
+  pa.idesc = ptx::idesc_f8f6f4((a.idesc >> 7) & 7u, (a.idesc >> 10) & 7u, 256, 256);
+  const int units = ((a.num_m_tiles + 1) / 2) * a.num_n_tiles;
+  cfg.gridDim = dim3(2 * (units < max_clusters ? units : max_clusters), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, pa) != cudaSuccess) return FP8Q_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
 template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC, int CM>
 int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                cudaStream_t stream) {
@@ -732,7 +985,7 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   const int BK = (tensor && BN == 256) ? kTensorBK : kBK;
   // The 256-wide per-tensor kernel runs in clusters of kTensorCM CTAs that
   // each load BN / kTensorCM rows of B's tile.
-  const int b_box_rows = (tensor && BN == 256) ? BN / kTensorCM : BN;
+  const int b_box_rows = (tensor && BN == 256) ? BN / (kTensorPair ? 2 : kTensorCM) : BN;
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, (uint32_t)BK, kBM) ||
       !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)BK, (uint32_t)b_box_rows))
@@ -764,6 +1017,14 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
 
   if (tensor) {
     constexpr int S256 = kTensorBK == 64 ? 9 : 4;   // ~216 KB or ~192 KB of ring
+    if (kTensorPair && BN == 256 && kTensorBK == 128) {
+      constexpr int PS = kPairStages, PA = kPairAcc;
+      if (vec)
+        return bf16 ? run_tensor_pair<PS, PA, true, true>(ta, tb, a, stream)
+                    : run_tensor_pair<PS, PA, false, true>(ta, tb, a, stream);
+      return bf16 ? run_tensor_pair<PS, PA, true, false>(ta, tb, a, stream)
+                  : run_tensor_pair<PS, PA, false, false>(ta, tb, a, stream);
+    }
     if (vec) {
       if (BN == 64)
         return bf16 ? run_tensor<64, 8, 128, true, true, 1>(ta, tb, a, grid, stream)

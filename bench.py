@@ -888,7 +888,7 @@ def main():
             "prequant": {"value": tf(ms_r_pre), "ms_per_step": ms_r_pre},
             "unit": "TFLOP/s",
             "gemm": {"achieved": r_gemm_tflops, "frac": r_gemm_tflops / fp8_peak_sust,
-                     "kernel": "gemm_tensor_kernel, vector-scale epilogue",
+                     "kernel": "gemm_tensor_pair_kernel (cta_group::2), row-scale epilogue",
                      "launches": r_gemm_n}},
         "context_pages_B300_ms_per_layer": {
             "fp8_current_autocast": 9.15, "fp8_current_prequant": 6.81,
@@ -919,8 +919,8 @@ def main():
         },
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,
                      "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_sust,
-                     "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_tensor_kernel"),
-                     "kernel": "gemm_tensor_kernel (12 GEMMs of the autocast step)",
+                     "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_tensor_pair_kernel"),
+                     "kernel": "gemm_tensor_pair_kernel, cta_group::2 (12 GEMMs of the autocast step)",
                      "launches": t_gemm_n, "peak_source": peak_src,
                      "frac_of_burst": t_gemm_tflops / fp8_peak_burst},
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,

@@ -264,6 +264,22 @@ int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C,
              int out_dtype, int64_t M, int64_t N, int64_t K,
              cudaStream_t stream);
 
+/* fp8_gemm, and in the same launch amax_out[0] = max |C[m, n]| over the
+ * values as stored (after the bf16 rounding for bf16 output); NaN propagates
+ * as in fp8_amax.  This is amax fused into the producer of the next
+ * quantisation: [te_blog] "Decoding the results for a real model" lists the
+ * extra memory pass that per-tensor amax needs among the overheads outside
+ * the GEMMs, and feeding amax_out to fp8_quantize_tensor as its `amax` spares
+ * the separate fp8_amax read of C.
+ *   amax_out: one device float, 4-byte aligned.  The call zeroes it on
+ *   `stream` first, so it holds exactly amax(C) when the GEMM is done
+ *   (0 when M, N or K is 0).
+ * Arguments, layout and errors otherwise as fp8_gemm (INVALID_ARG also for a
+ * null amax_out, MISALIGNED for an unaligned one). */
+int fp8_gemm_amax(const fp8q_operand *A, const fp8q_operand *B, void *C,
+                  int out_dtype, int64_t M, int64_t N, int64_t K,
+                  float *amax_out, cudaStream_t stream);
+
 /* The three GEMMs of a linear layer y = x w^T with x [M, K] (tokens x input
  * features), w [N, K], grad_out g [M, N] ([fp8_parity] FP8Matmul; [te_blog]
  * "Fprop, Dgrad, and Wgrad shapes are all benchmarked individually").  M, N, K

@@ -47,7 +47,7 @@ EXPORTS = (
     "fp8q_selftest_barrier_timeout", "fp8_amax",
     "fp8_quantize_tensor", "fp8_quantize_delayed", "fp8q_history_init",
     "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_block128x128", "fp8_gemm",
-    "fp8_gemm_fprop",
+    "fp8_gemm_amax", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
     "fp8_linear_autocast_noalloc",
 )
@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_block128x128": (I32, [P, I32, I64, I64, I32, P, P, P, I32, P]),
             "fp8_gemm": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+            "fp8_gemm_amax": (I32, [OP, OP, P, I32, I64, I64, I64, P, P]),
             "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_dgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_wgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
@@ -345,6 +346,19 @@ def fp8_gemm(A: GemmOperand, B: GemmOperand, out_dtype=torch.bfloat16, out=None,
     M, N = A.rows, B.rows
     out = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=A.data.device)
     return _gemm_call("fp8_gemm", A, B, out, M, N, A.K, stream)
+
+
+def fp8_gemm_amax(A: GemmOperand, B: GemmOperand, out_dtype=torch.bfloat16, out=None,
+                  amax=None, stream=None):
+    """fp8_gemm plus amax(|C|) over the stored output from the same launch.
+    Returns (C, amax) with amax a one-element fp32 device tensor."""
+    M, N = A.rows, B.rows
+    out = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=A.data.device)
+    amax = amax if amax is not None else _empty((1,), torch.float32, A.data)
+    _check(lib().fp8_gemm_amax(ctypes.byref(A.struct), ctypes.byref(B.struct), _ptr(out),
+                               _out_dtype(out.dtype), M, N, A.K, _ptr(amax), _stream(stream)),
+           "fp8_gemm_amax")
+    return out, amax
 
 
 def fp8_gemm_fprop(x: GemmOperand, w: GemmOperand, out_dtype=torch.bfloat16, out=None,

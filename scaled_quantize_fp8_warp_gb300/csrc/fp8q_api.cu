@@ -376,8 +376,10 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t
   return from_cuda(launch_quant2d(p, stream));
 }
 
-int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t M,
-             int64_t N, int64_t K, cudaStream_t stream) {
+namespace {
+
+int gemm_common(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t M,
+                int64_t N, int64_t K, float *amax_out, cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 0 || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
   if (N % 16 != 0 || K % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   int rc;
@@ -392,7 +394,24 @@ int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtyp
     fprintf(stderr, "[fp8q] gemm M=%lld N=%lld K=%lld A(fmt=%d,scale=%d) B(fmt=%d,scale=%d) out=%d\n",
             (long long)M, (long long)N, (long long)K, A->format, A->scaling, B->format,
             B->scaling, out_dtype);
-  return launch_gemm(to_dev(A), to_dev(B), C, out_dtype, M, N, K, stream);
+  if (amax_out != nullptr &&
+      cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
+    return FP8Q_ERR_CUDA;
+  return launch_gemm(to_dev(A), to_dev(B), C, out_dtype, M, N, K, stream, amax_out);
+}
+
+}  // namespace
+
+int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t M,
+             int64_t N, int64_t K, cudaStream_t stream) {
+  return gemm_common(A, B, C, out_dtype, M, N, K, nullptr, stream);
+}
+
+int fp8_gemm_amax(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype,
+                  int64_t M, int64_t N, int64_t K, float *amax_out, cudaStream_t stream) {
+  if (amax_out == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(amax_out) & 3u) return FP8Q_ERR_MISALIGNED;
+  return gemm_common(A, B, C, out_dtype, M, N, K, amax_out, stream);
 }
 
 int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y, int out_dtype,

@@ -84,6 +84,7 @@ struct GemmArgs {
   int64_t a_stride_row, a_stride_k;
   int64_t b_stride_row, b_stride_k;
   int a_row, b_row;   // per-tensor kernel: 1 = one scale per row (ROW), 0 = scalar
+  unsigned int *amax;  // max |C| over the stored values (fp32 bit pattern), or null
   unsigned int *err;
 };
 
@@ -214,10 +215,13 @@ __device__ __forceinline__ void drain_mma(uint32_t drain_bar, volatile int *abor
 }
 
 // Store 32 consecutive fp32 results (already scaled) of row m starting at
-// column n0; columns >= N are skipped in groups of 8 (N % 16 == 0).
+// column n0; columns >= N are skipped in groups of 8 (N % 16 == 0).  Returns
+// max |value| over what was stored, as it was stored (bf16 rounded or fp32),
+// as an fp32 bit pattern; NaN patterns sort above Inf.
 template <bool OUT_BF16>
-__device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n0,
-                                        const float (&v)[32]) {
+__device__ __forceinline__ uint32_t store32(void *C, int64_t N, int64_t m, int64_t n0,
+                                            const float (&v)[32]) {
+  uint32_t mx = 0;
   if (OUT_BF16) {
     __nv_bfloat16 *row = static_cast<__nv_bfloat16 *>(C) + m * N;
 #pragma unroll
@@ -230,17 +234,32 @@ __device__ __forceinline__ void store32(void *C, int64_t N, int64_t m, int64_t n
           w[h] = *reinterpret_cast<uint32_t *>(&b);
         }
         *reinterpret_cast<uint4 *>(row + n0 + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+        const uint32_t k = 0x7FFF7FFFu;
+        const uint32_t p = __vmaxu2(__vmaxu2(w[0] & k, w[1] & k), __vmaxu2(w[2] & k, w[3] & k));
+        mx = max(mx, max(p & 0xFFFFu, p >> 16) << 16);
       }
     }
   } else {
     float *row = static_cast<float *>(C) + m * N;
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-      if (n0 + 4 * g < N)
+      if (n0 + 4 * g < N) {
         *reinterpret_cast<float4 *>(row + n0 + 4 * g) =
             make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mx = max(mx, __float_as_uint(v[4 * g + j]) & 0x7FFFFFFFu);
+      }
     }
   }
+  return mx;
+}
+
+// One atomicMax per warp of the lanes' running output maxima (the warp is
+// converged here), when the caller asked for amax(C).
+__device__ __forceinline__ void publish_amax(unsigned int *amax, uint32_t run_max) {
+  if (amax == nullptr) return;
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run_max);
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax, m);
 }
 
 // ------------------------------------------------------------------------
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(192, 1)
     // Per-tensor: one product s_A s_B.  With row scales (VEC): s_A of this
     // thread's row times s_B of each column, applied the same way.
     const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
-    uint32_t acc_it = 0;
+    uint32_t acc_it = 0, run_max = 0;
     for (int u = unit0; u < total; u += unit_step, ++acc_it) {
       int mu, nt;
       tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / CM);
@@ -365,12 +384,13 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
         }
-        if (m < p.M && n0 < p.N) store32<OUT_BF16>(p.C, p.N, m, n0, v);
+        if (m < p.M && n0 < p.N) run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * buf);
     }
+    publish_amax(p.amax, run_max);
   }
 
   tc_fence_before();
@@ -537,7 +557,7 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp & 3;
     const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
     const uint32_t acce_even0 = mapa_shared(acce0, 0);
-    uint32_t acc_it = 0;
+    uint32_t acc_it = 0, run_max = 0;
     for (int u = unit0; u < total; u += unit_step, ++acc_it) {
       int mu, nt;
       tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / 2);
@@ -568,7 +588,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(r[j]), scale);
         }
-        if (m < p.M && n0 < p.N) store32<OUT_BF16>(p.C, p.N, m, n0, v);
+        if (m < p.M && n0 < p.N) run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
       }
       tc_fence_before();
       __syncwarp();
@@ -579,6 +599,7 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_cluster(acce_even0 + 8 * buf);
       }
     }
+    publish_amax(p.amax, run_max);
   }
 
   tc_fence_before();
@@ -706,7 +727,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     float *my_bs = sh_bscale[pw];
     constexpr int kPerLane = C / 32;      // B tile scales each lane stages (2 or 4)
-    uint32_t it = 0;
+    uint32_t it = 0, run_max = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int mt, nt;
@@ -804,11 +825,12 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
             float v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
-            store32<OUT_BF16>(p.C, p.N, m, n0, v);
+            run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
           }
         }
       }
     }
+    publish_amax(p.amax, run_max);
   }
 
   tc_fence_before();
@@ -959,7 +981,7 @@ bool make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, u
 }
 
 int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int out_dtype,
-                int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+                int64_t M, int64_t N, int64_t K, cudaStream_t stream, float *amax_out) {
   const bool bf16 = out_dtype == FP8Q_DT_BF16;
   if (M == 0 || N == 0) return FP8Q_OK;
   if (K == 0) {
@@ -1008,6 +1030,7 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   a.b_stride_k = B.stride_k;
   a.a_row = A.scaling == FP8Q_SCALE_ROW ? 1 : 0;
   a.b_row = B.scaling == FP8Q_SCALE_ROW ? 1 : 0;
+  a.amax = reinterpret_cast<unsigned int *>(amax_out);
   a.err = device_error_word();
   if (a.err == nullptr) return FP8Q_ERR_CUDA;
   const int64_t tiles = (int64_t)a.num_m_tiles * a.num_n_tiles;

@@ -66,9 +66,11 @@ struct GemmOperandDev {
   int64_t stride_k;
 };
 
-// C[M,N] = A[M,K] . B[N,K]^T with dequantising scales.
+// C[M,N] = A[M,K] . B[N,K]^T with dequantising scales.  With amax_out (one
+// fp32, zero on entry) the epilogue also folds max |C| over the stored values
+// into it.
 int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C,
                 int out_dtype, int64_t M, int64_t N, int64_t K,
-                cudaStream_t stream);
+                cudaStream_t stream, float *amax_out = nullptr);
 
 }  // namespace fp8q

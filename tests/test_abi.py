@@ -119,6 +119,13 @@ def test_validation_before_device(lib):
     bad = fq.Operand(0x10000, fq.E4M3, 9, 0x20000, 0, 0)
     assert lib.fp8_gemm(ctypes.byref(bad), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32, 32,
                         None) == 1
+    # gemm with fused amax: needs a 4-byte aligned amax, then validates as fp8_gemm
+    assert lib.fp8_gemm_amax(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32,
+                             32, None, None) == 1
+    assert lib.fp8_gemm_amax(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32,
+                             32, P(0x10002), None) == 2
+    assert lib.fp8_gemm_amax(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 24,
+                             32, aligned, None) == 1
     # autocast: workspace too small
     assert lib.fp8_linear_autocast(aligned, aligned, fq.DT_BF16, 32, 32, 32, 0, None, None,
                                    aligned, fq.DT_BF16, aligned, 16, None) == 4

@@ -421,3 +421,79 @@ def test_rowwise_all_roles_full_size(fq):
         ms, ns = _sample_points(Rr, Cc, rng, n=2048)
         yr, ab = oracle.gemm_points(opA, opB, ms, ns)
         check_bound(f32(got)[ms, ns], yr, ab, True, nm)
+
+
+# ------------------------------------------------------------- fused amax
+
+def _amax_operands(fq, M, N, K, kind, seed):
+    a = workloads.normal((M, K), 1.0, seed).cuda()
+    b = workloads.normal((N, K), 0.02, seed + 1).cuda()
+    if kind == "tensor":
+        qa, _, sa = fq.fp8_quantize_tensor(a, 0, fq.fp8_amax(a))
+        qb, _, sb = fq.fp8_quantize_tensor(b, 0, fq.fp8_amax(b))
+        return fq.GemmOperand.tensor(qa, 0, sa), fq.GemmOperand.tensor(qb, 0, sb)
+    if kind == "row":
+        qa, sa, _, _ = fq.fp8_quantize_rowwise(a, 0)
+        qb, sb, _, _ = fq.fp8_quantize_rowwise(b, 0)
+        return fq.GemmOperand.row(qa, 0, sa), fq.GemmOperand.row(qb, 0, sb)
+    qa, sa, _, _ = fq.fp8_quantize_tile1x128(a, 0)
+    qb, _, sb = fq.fp8_quantize_block128x128(b, 0)
+    return fq.GemmOperand.tile(qa, 0, sa), fq.GemmOperand.block(qb, 0, sb)
+
+
+@pytest.mark.parametrize("M,N,K,kind", [
+    (300, 272, 400, "tensor"),   # CTA-pair kernel, ragged M and K, odd M-tile count
+    (129, 64, 256, "tensor"),    # one-SM kernel, 64-wide tiles
+    (257, 128, 512, "row"),      # one-SM kernel, 128-wide tiles, row scales
+    (640, 528, 384, "row"),      # CTA-pair kernel, row scales, ragged N
+    (384, 272, 640, "block"),    # block-scaled kernel
+])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_gemm_fused_amax(fq, M, N, K, kind, out_dtype):
+    """amax from the GEMM epilogue equals fp8_amax of the stored output, bit
+    for bit, and the output itself equals plain fp8_gemm's."""
+    A, B = _amax_operands(fq, M, N, K, kind, 90)
+    y, am = fq.fp8_gemm_amax(A, B, out_dtype=out_dtype)
+    y2 = fq.fp8_gemm(A, B, out_dtype=out_dtype)
+    ref = fq.fp8_amax(y)
+    gpu_status_ok(fq)
+    iv = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
+    assert torch.equal(y.view(iv), y2.view(iv)), "fused amax changed the GEMM output"
+    assert_f32_bits_equal(f32(am), f32(ref), "fused amax")
+    assert f32(am)[0] == np.float32(y.float().abs().max().item())
+
+
+def test_gemm_fused_amax_resets_between_calls(fq):
+    """The call zeroes its amax first: a second, smaller product reports its
+    own maximum, not the first call's."""
+    A, B = _amax_operands(fq, 512, 512, 512, "tensor", 92)
+    y, am = fq.fp8_gemm_amax(A, B)
+    big = f32(am)[0]
+    qa = A.data
+    small = fq.GemmOperand.tensor(qa, 0, (A.scale * 1e-3).contiguous())
+    y2, am2 = fq.fp8_gemm_amax(small, B, out=y, amax=am)
+    gpu_status_ok(fq)
+    assert f32(am2)[0] == np.float32(y2.float().abs().max().item())
+    assert f32(am2)[0] < big
+
+
+def test_gemm_fused_amax_empty(fq):
+    A, B = _amax_operands(fq, 128, 128, 128, "tensor", 93)
+    am = torch.full((1,), 5.0, device="cuda")
+    empty = fq.GemmOperand.tensor(A.data[:0], 0, A.scale)
+    y, am = fq.fp8_gemm_amax(empty, B, amax=am)
+    gpu_status_ok(fq)
+    assert y.shape == (0, 128) and f32(am)[0] == 0.0
+
+
+def test_gemm_fused_amax_full_size_qkv_fprop(fq):
+    """QKV Fprop of the layer (15872 x 12288 x 4096) through the CTA-pair kernel."""
+    shape = workloads.LAYER[0]
+    x, w, _ = workloads.layer_inputs(shape, 0)
+    xd, wd = x.cuda(), w.cuda()
+    qx, _, sx = fq.fp8_quantize_tensor(xd, 0, fq.fp8_amax(xd))
+    qw, _, sw = fq.fp8_quantize_tensor(wd, 0, fq.fp8_amax(wd))
+    y, am = fq.fp8_gemm_amax(fq.GemmOperand.tensor(qx, 0, sx), fq.GemmOperand.tensor(qw, 0, sw))
+    ref = fq.fp8_amax(y)
+    gpu_status_ok(fq)
+    assert_f32_bits_equal(f32(am), f32(ref), "fused amax")

@@ -386,6 +386,7 @@ class Runner:
         self.tops = state.tensor_operands()
         self.rops = state.row_operands()
         self.gemm_events = None   # list of (start, end, flops) when recording
+        self._cin, self._cout = self.torch.cuda.Stream(), self.torch.cuda.Stream()
 
     def _gemm(self, role, A, B, C):
         fq, torch = self.fq, self.torch
@@ -494,8 +495,6 @@ class Runner:
         its compute; everything is ordered after the step's start on the
         compute stream, and the compute stream waits for the last copy-out)."""
         torch, fq, st = self.torch, self.fq, self.stream
-        if not hasattr(self, "_cin"):
-            self._cin, self._cout = torch.cuda.Stream(), torch.cuda.Stream()
         start = torch.cuda.Event()
         start.record(st)
         self._cin.wait_event(start)
@@ -785,7 +784,7 @@ def main():
             xA, wB, out=y0, amax=am_y, stream=stream), K, W, clk=clk)
 
     # ---- end to end through host buffers (headline recipe)
-    ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), 1)
+    ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), W)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
     xq, _ = workloads.quantize_activation()

@@ -49,6 +49,8 @@ struct QuantParams {
   float *q_scales;             // tile: [ceil(cols/128), rows]; block: [nrb, ncb]
   float *qt_scales;            // tile: [ceil(rows/128), cols]
   unsigned int *err;           // device error word (bounded waits)
+  int work_slot;               // tile-scheduling slot (set at launch)
+  int dynamic;                 // 1: tiles past the first few are claimed (set at launch)
 };
 
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,

@@ -25,6 +25,8 @@
 // byte transpose (uniform scales) or a second cast (column-tile scales).
 #include <cuda.h>
 #include <cuda_fp8.h>
+
+#include <atomic>
 #include <stdint.h>
 #include <string.h>
 
@@ -59,14 +61,6 @@ __device__ __forceinline__ uint32_t abs_bits(float v) {
 __device__ __forceinline__ float scale_from_amax(float amax, float fm) {
   float s = __fdiv_rn(amax, fm);
   return (s < 1e-12f) ? 1e-12f : s;
-}
-
-// Correctly rounded x / s given r = RN(1/s) (see the file comment).
-__device__ __forceinline__ float div_fast(float x, float s, float r) {
-  float q0 = __fmul_rn(x, r);
-  float e = __fmaf_rn(-q0, s, x);
-  float q1 = __fmaf_rn(e, r, q0);
-  return copysignf(q1, q0);
 }
 
 // Two fp32 values -> two FP8 bytes (lo in the low byte), RNE, saturating.
@@ -314,10 +308,19 @@ enum KernelMode : int {
   kKRowCast = 7     // row-wise pass 2: cast with the scales of those amaxes
 };
 
+// Dynamic tile scheduling: each launch of the quantize kernel takes one slot
+// (round-robin over kQuantWorkSlots, so launches that overlap in time use
+// different slots); work[0] hands out tile indices, work[1] counts CTAs that
+// are done, and the last CTA returns both to zero for the slot's next launch.
+constexpr int kQuantWorkSlots = 256;
+__device__ unsigned int g_quant_work[2 * kQuantWorkSlots];
+
 // Input tiles (128 x 128 elements) reach shared memory by TMA through a ring
-// of kStages buffers; thread 0 refills a buffer as soon as every thread has
-// copied its part of the previous tile out of it, so up to kStages tiles per
-// CTA are in flight while earlier ones are converted and stored.
+// of kStages buffers; thread 0 claims the next tile and refills a buffer as
+// soon as every thread has copied its part of the previous tile out of it, so
+// up to kStages tiles per CTA are in flight while earlier ones are converted
+// and stored.  Claiming tiles as CTAs free up (rather than a fixed stride)
+// evens out SMs that stream at different rates.
 template <typename InT>
 struct QuantRing {
   static constexpr int kTileBytes = 128 * 128 * (int)sizeof(InT);
@@ -341,6 +344,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   __shared__ uint32_t sh_colmax[8][128];
   __shared__ uint32_t sh_red[8];
   __shared__ __align__(8) uint64_t sh_full[Ring::kStages];
+  __shared__ int sh_tr[Ring::kStages], sh_tc[Ring::kStages];  // tile of a stage; -1: none
   __shared__ int sh_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -355,24 +359,37 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   const uint8_t *ring_ptr = dyn_smem + (ring - raw);
   volatile int *abort_flag = &sh_abort;
 
-  // Tiles of this CTA: blockIdx.x + i * gridDim.x.  Per-tensor current
-  // scaling runs right after the amax pass over the same data, so it walks
-  // the tiles backwards and meets the most recently read (still L2-resident)
-  // part of x first.
-  const int64_t my_tiles =
-      (blockIdx.x < ntiles) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  auto tile_of = [&](int64_t i) -> int64_t {
-    const int64_t t = blockIdx.x + i * gridDim.x;
-    return (KM == kKTensor) ? (ntiles - 1 - t) : t;
-  };
-  auto issue = [&](int64_t i) {
+  // Per-tensor current scaling runs right after the amax pass over the same
+  // data, so it hands out the tiles backwards and meets the most recently read
+  // (still L2-resident) part of x first.
+  unsigned int *work = &g_quant_work[2 * p.work_slot];
+  unsigned int next_claim = 0;  // thread 0: claimed, not yet issued
+  // Work order: a CTA's first kStages tiles are blockIdx.x + j * gridDim.x
+  // (loaded at once).  With p.dynamic every later tile is claimed from the
+  // slot's counter, numbered on from kStages * gridDim.x; otherwise the fixed
+  // stride continues (few tiles per CTA leave little tail to even out, and
+  // the claims' cost would show).
+  // thread 0: start the load of pipeline step i for tile number c; a step past
+  // the last tile carries -1 and completes with no data.  Claims are made one
+  // step ahead of their use, so the atomic's round trip overlaps a tile's
+  // work.  One CTA's tile numbers only grow (one thread's claims on one
+  // address come back in increasing order), so after a -1 every later step
+  // is -1 as well.
+  auto issue_tile = [&](int64_t i, int64_t c) {
     const int s = (int)(i % Ring::kStages);
-    const int64_t tt = tile_of(i);
-    const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
     const uint32_t bar = ptx::smem_u32(&sh_full[s]);
-    ptx::mbar_arrive_expect_tx(bar, Ring::kTileBytes);
-    ptx::tma_load_2d(ring + s * Ring::kTileBytes, &tmx, (int32_t)(tc * 128), (int32_t)(tr * 128),
-                     bar);
+    if (c < ntiles) {
+      const int64_t t = (KM == kKTensor) ? ntiles - 1 - c : c;
+      const int tr = (int)(t / tiles_c);
+      const int tc = (int)(t - (int64_t)tr * tiles_c);
+      sh_tr[s] = tr;
+      sh_tc[s] = tc;
+      ptx::mbar_arrive_expect_tx(bar, Ring::kTileBytes);
+      ptx::tma_load_2d(ring + s * Ring::kTileBytes, &tmx, tc * 128, tr * 128, bar);
+    } else {
+      sh_tr[s] = -1;
+      ptx::mbar_arrive(bar);
+    }
   };
 
   if (tid == 0) {
@@ -380,8 +397,11 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     sh_abort = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
-    if (my_tiles > 0) ptx::prefetch_tmap(&tmx);
-    for (int64_t i = 0; i < my_tiles && i < Ring::kStages; ++i) issue(i);
+    ptx::prefetch_tmap(&tmx);
+#pragma unroll
+    for (int j = 0; j < Ring::kStages; ++j)
+      issue_tile(j, (int64_t)blockIdx.x + (int64_t)j * gridDim.x);
+    if (p.dynamic) next_claim = atomicAdd(&work[0], 1u);
   }
   __syncthreads();
 
@@ -397,17 +417,17 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     r_u = __fdiv_rn(1.0f, s_u);
   }
   uint32_t run_max = 0;  // delayed: running max |x| of this CTA
-  int64_t issued = my_tiles < Ring::kStages ? my_tiles : Ring::kStages;  // thread 0's count
+  int64_t issued = Ring::kStages;  // thread 0's count of claimed pipeline steps
 
-  // Every thread runs every iteration (and every __syncthreads) even after an
-  // abort; an aborted CTA only skips the work.
-  for (int64_t i = 0; i < my_tiles; ++i) {
+  // Every thread takes every iteration's barriers; the loop ends for all
+  // threads at once (a CTA-wide abort verdict, or a stage without a tile).
+  for (int64_t i = 0;; ++i) {
     const int s = (int)(i % Ring::kStages);
     const uint32_t parity = (uint32_t)((i / Ring::kStages) & 1);
     const bool ok = ptx::wait_bounded_warp(ptx::smem_u32(&sh_full[s]), parity, abort_flag, p.err);
-    const int64_t tt = tile_of(i);
-    const int64_t tr = tt / tiles_c, tc = tt - tr * tiles_c;
-    const int64_t r0 = tr * 128, c0 = tc * 128;
+    const int tr = ok ? *reinterpret_cast<volatile int *>(&sh_tr[s]) : -1;
+    const int tc = ok ? *reinterpret_cast<volatile int *>(&sh_tc[s]) : 0;
+    const int64_t r0 = (int64_t)tr * 128, c0 = (int64_t)tc * 128;
     const int64_t cbase = c0 + cg * 8;
     const int64_t rbase = r0 + rg * 8;
     const bool col_ok = cbase < cols;
@@ -419,19 +439,22 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     const uint8_t *tile_ptr = ring_ptr + s * Ring::kTileBytes;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      if (ok) v[r].load_smem(tile_ptr + ((rg * 8 + r) * 128 + cg * 8) * (int)sizeof(InT));
+      if (ok && tr >= 0) v[r].load_smem(tile_ptr + ((rg * 8 + r) * 128 + cg * 8) * (int)sizeof(InT));
       else v[r].zero();
     }
-    // One CTA-wide verdict (every thread takes the same branch below, so the
-    // __syncthreads sequence stays identical); this barrier also frees buffer s.
+    // One CTA-wide verdict, so every thread leaves the loop at the same
+    // iteration; this barrier also frees buffer s.  All threads read the same
+    // stage tile, so `tr < 0` is uniform too.
     const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
-    if (tid == 0 && i + Ring::kStages < my_tiles && !*abort_flag) {
-      issue(i + Ring::kStages);
+    if (!all_ok || tr < 0) break;
+    if (tid == 0 && !*abort_flag) {
+      if (p.dynamic) {
+        issue_tile(i + Ring::kStages, (int64_t)Ring::kStages * gridDim.x + next_claim);
+        next_claim = atomicAdd(&work[0], 1u);
+      } else {
+        issue_tile(i + Ring::kStages, (int64_t)blockIdx.x + (i + Ring::kStages) * gridDim.x);
+      }
       issued = i + Ring::kStages + 1;
-    }
-    if (!all_ok) {
-      __syncthreads();
-      continue;
     }
 
     uint32_t rowmax[8];
@@ -651,17 +674,29 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
         }
       }
     }
-    __syncthreads();  // shared scratch is reused by the next tile
+    // Shared scratch that crosses warps is reused by the next tile.  Per-tensor,
+    // delayed and 1x128 row-tile casts keep theirs per warp (ordered by the
+    // barrier at the top of the next iteration).
+    if (!(KM == kKTensor || KM == kKDelayed || KM == kKTileRow)) __syncthreads();
   }
 
-  if (*abort_flag && tid == 0) {
-    // Let copies still in flight land before the CTA exits (bounded).
-    for (int64_t j = (issued > Ring::kStages ? issued - Ring::kStages : 0); j < issued; ++j) {
-      const uint32_t bar = ptx::smem_u32(&sh_full[j % Ring::kStages]);
-      const uint32_t par = (uint32_t)((j / Ring::kStages) & 1);
-      const uint64_t t0 = ptx::globaltimer_ns();
-      while (!ptx::mbar_try_wait(bar, par) && ptx::globaltimer_ns() - t0 < 200000000ull) {
+  if (tid == 0) {
+    if (*abort_flag) {
+      // Let copies still in flight land before the CTA exits (bounded).
+      for (int64_t j = (issued > Ring::kStages ? issued - Ring::kStages : 0); j < issued; ++j) {
+        const uint32_t bar = ptx::smem_u32(&sh_full[j % Ring::kStages]);
+        const uint32_t par = (uint32_t)((j / Ring::kStages) & 1);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (!ptx::mbar_try_wait(bar, par) && ptx::globaltimer_ns() - t0 < 200000000ull) {
+        }
       }
+    }
+    // Every claim of this CTA precedes its "done"; the last CTA resets the slot.
+    if (p.dynamic) __threadfence();
+    if (p.dynamic && atomicAdd(&work[1], 1u) == gridDim.x - 1) {
+      work[0] = 0u;
+      work[1] = 0u;
+      __threadfence();
     }
   }
 
@@ -780,10 +815,15 @@ cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
                     (uint64_t)p.cols, (uint64_t)p.rows, (uint64_t)p.cols * sizeof(InT), 128, 128,
                     CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  if (ntiles > 0x7FFFFFFF) return cudaErrorInvalidValue;  // tile indices are 32-bit
   int64_t grid = (int64_t)sm_count() * blocks_per_sm;
   if (ntiles < grid) grid = ntiles;
   if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, kQuantThreads, Ring::kSmemBytes, stream>>>(tmx, p);
+  static std::atomic<unsigned int> next_slot{0};
+  QuantParams q = p;
+  q.dynamic = ntiles >= 8 * grid ? 1 : 0;
+  q.work_slot = q.dynamic ? (int)(next_slot.fetch_add(1u) % kQuantWorkSlots) : 0;
+  kernel<<<(unsigned)grid, kQuantThreads, Ring::kSmemBytes, stream>>>(tmx, q);
   return cudaGetLastError();
 }
 

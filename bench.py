@@ -787,7 +787,7 @@ def main():
     ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), W)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
-    xq, _ = workloads.quantize_activation()
+    xq, out_rows = workloads.quantize_activation()
     xq = xq.cuda()
     R, C = xq.shape
     n = R * C
@@ -815,7 +815,9 @@ def main():
         xq, fq.E4M3, rows=True, q=qt, q_scales=st, stream=stream), QK, W, flush=flush)
     ms_amax = time_steps(torch, dist, stream, lambda: fq.fp8_amax(xq, out=am, stream=stream),
                          QK, W, flush=flush)
-    ms_tensor = time_steps(torch, dist, stream, lambda: (
+    ms_tensor = time_steps(torch, dist, stream, lambda: fq.fp8_quantize_tensor_current(
+        xq, fq.E4M3, q=qt, amax=am, scale=sc, stream=stream), QK, W, flush=flush)
+    ms_tensor_2k = time_steps(torch, dist, stream, lambda: (
         fq.fp8_amax(xq, out=am, stream=stream),
         fq.fp8_quantize_tensor(xq, fq.E4M3, am, q=qt, scale=sc, stream=stream)), QK, W,
         flush=flush)
@@ -831,11 +833,28 @@ def main():
     ms_row2 = time_steps(torch, dist, stream, lambda: fq.fp8_quantize_rowwise(
         xq, fq.E4M3, rows=True, cols=True, q=qt, q_scales=rs_r, q_t=qtt, qt_scales=rs_c,
         stream=stream), QK, W, flush=flush)
-    ms_tensor2 = time_steps(torch, dist, stream, lambda: (
-        fq.fp8_amax(xq, out=am, stream=stream),
-        fq.fp8_quantize_tensor(xq, fq.E4M3, am, want_q=True, want_qt=True, q=qt, q_t=qtt,
-                               scale=sc, stream=stream)), QK, W, flush=flush)
+    ms_tensor2 = time_steps(torch, dist, stream, lambda: fq.fp8_quantize_tensor_current(
+        xq, fq.E4M3, want_q=True, want_qt=True, q=qt, q_t=qtt, amax=am, scale=sc,
+        stream=stream), QK, W, flush=flush)
     dual_bytes = n * 2 + 2 * n     # read x once, write q and q_t (scales are < 0.1%)
+
+    # ---- accuracy on the same activation: MSE of the dequantised values on
+    # the rows without outliers, 1x128 tiles against one scale per tensor
+    # (analysis of the kernels' outputs, outside every timed region)
+    keep = torch.ones(R, dtype=torch.bool, device=xq.device)
+    keep[out_rows.to(xq.device)] = False
+    xf = xq.float()
+    fq.fp8_quantize_tile1x128(xq, fq.E4M3, rows=True, q=qt, q_scales=st, stream=stream)
+    fq.fp8_amax(xq, out=am, stream=stream)
+    qtt2 = torch.empty_like(qt)
+    fq.fp8_quantize_tensor(xq, fq.E4M3, am, q=qtt2, scale=sc, stream=stream)
+    torch.cuda.synchronize()
+    deq_tile = (qt.view(torch.float8_e4m3fn).float().view(R, C // 128, 128)
+                * st.t().reshape(R, C // 128, 1)).view(R, C)
+    deq_tensor = qtt2.view(torch.float8_e4m3fn).float() * sc
+    mse_tile = ((deq_tile - xf)[keep] ** 2).mean().item()
+    mse_tensor = ((deq_tensor - xf)[keep] ** 2).mean().item()
+    del xf, deq_tile, deq_tensor, qtt2
     gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
 
     # ---- CPU baseline (oracle on the host cores, rank 0, N = 1 only)
@@ -921,11 +940,15 @@ def main():
                      "frac": gbps(2 * n, ms_amax) / hbm_peak},
             "tensor_current": {"GB/s (over 3 B/elem)": gbps(3 * n, ms_tensor),
                                "us": ms_tensor * 1e3,
-                               "frac": gbps(3 * n, ms_tensor) / hbm_peak},
+                               "frac": gbps(3 * n, ms_tensor) / hbm_peak,
+                               "how": ("fp8_quantize_tensor_current: amax pass, grid barrier and "
+                                       "cast from L2 in one cooperative launch"),
+                               "two_kernels_us": ms_tensor_2k * 1e3},
             "both_orientations": {
                 "note": ("q and q_t from one call; GB/s over the unique bytes (2 B read + "
                          "2 B written per element); row-wise and per-tensor read x twice "
-                         "(amax pass, then cast), the second read mostly from L2"),
+                         "(amax pass, then cast), the second read mostly from L2 (per-tensor: "
+                         "one cooperative launch)"),
                 "tile1x128_rows_and_cols": {"GB/s": gbps(dual_bytes, ms_tile2),
                                             "us": ms_tile2 * 1e3,
                                             "frac": gbps(dual_bytes, ms_tile2) / hbm_peak},
@@ -933,6 +956,10 @@ def main():
                             "frac": gbps(dual_bytes, ms_row2) / hbm_peak},
                 "tensor_current": {"GB/s": gbps(dual_bytes, ms_tensor2), "us": ms_tensor2 * 1e3,
                                    "frac": gbps(dual_bytes, ms_tensor2) / hbm_peak}},
+            "accuracy": {"mse_rows_without_outliers": {"tile1x128": mse_tile,
+                                                       "tensor": mse_tensor},
+                         "rows": int(keep.sum().item()),
+                         "note": "dequantised E4M3 vs the bf16 input; 1x128 tiles should be lower"},
             "unit": "GB/s", "peak": hbm_peak,
         },
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,

@@ -161,6 +161,24 @@ int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows,
                         float *scale_out, uint8_t *q, uint8_t *q_t,
                         int saturate, cudaStream_t stream);
 
+/* Per-tensor current scaling in one call: *amax_out = max |x| (as fp8_amax),
+ * then the cast of fp8_quantize_tensor with that amax ([fp8_parity]
+ * scaled_roundtrip with scale=None: amax, scale and cast together).  Results
+ * are those of fp8_amax followed by fp8_quantize_tensor, bit for bit.
+ *   When x holds at most 80 MiB (it then stays in the L2 cache between the
+ *   two passes) both run in one cooperative launch: the amax pass reads x,
+ *   a grid-wide barrier publishes the amax, and the cast re-reads x from L2.
+ *   Larger inputs run the two kernels.
+ *   amax_out   device float, 4-byte aligned: receives max |x| (zeroed on
+ *              `stream` first)
+ *   the other arguments as fp8_quantize_tensor.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA (including a cooperative
+ * launch the device refuses). */
+int fp8_quantize_tensor_current(const void *x, int in_dtype, int64_t rows,
+                                int64_t cols, int format, float *amax_out,
+                                float *scale_out, uint8_t *q, uint8_t *q_t,
+                                int saturate, cudaStream_t stream);
+
 /* Per-tensor delayed scaling ([fp8_parity] smoke step 3; [te_blog]
  * DelayedScaling "relies on an amax history"): s = max(fl32(max(hist->amax) /
  * fmax), 1e-12) is computed from the history alone, x is cast with s, then

@@ -45,7 +45,8 @@ LIB_PATH = os.path.join(_PKG, "_build", "libfp8q.so")
 EXPORTS = (
     "fp8q_status_string", "fp8q_device_status", "fp8q_device_supported",
     "fp8q_selftest_barrier_timeout", "fp8_amax",
-    "fp8_quantize_tensor", "fp8_quantize_delayed", "fp8q_history_init",
+    "fp8_quantize_tensor", "fp8_quantize_tensor_current", "fp8_quantize_delayed",
+    "fp8q_history_init",
     "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_block128x128", "fp8_gemm",
     "fp8_gemm_amax", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
@@ -91,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8_amax": (I32, [P, I32, I64, P, P]),
             "fp8_quantize_tensor": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_delayed": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+            "fp8_quantize_tensor_current": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8q_history_init": (I32, [P, P, P]),
             "fp8_quantize_tile1x128": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
@@ -192,6 +194,24 @@ def fp8_quantize_tensor(x, fmt, amax, want_q=True, want_qt=False, saturate=False
                                      _ptr(q if want_q else None), _ptr(q_t if want_qt else None),
                                      int(saturate), _stream(stream)), "fp8_quantize_tensor")
     return (q if want_q else None), (q_t if want_qt else None), scale
+
+
+def fp8_quantize_tensor_current(x, fmt, want_q=True, want_qt=False, saturate=False, q=None,
+                                q_t=None, amax=None, scale=None, stream=None):
+    """amax and per-tensor cast in one call (one cooperative launch when x
+    fits in L2).  Returns (q | None, q_t | None, amax [1], scale [1])."""
+    R, C = _rows_cols(x)
+    if want_q and q is None:
+        q = _empty((R, C), torch.uint8, x)
+    if want_qt and q_t is None:
+        q_t = _empty((C, R), torch.uint8, x)
+    amax = amax if amax is not None else _empty((1,), torch.float32, x)
+    scale = scale if scale is not None else _empty((1,), torch.float32, x)
+    _check(lib().fp8_quantize_tensor_current(
+        _ptr(x), _in_dtype(x), R, C, fmt, _ptr(amax), _ptr(scale), _ptr(q if want_q else None),
+        _ptr(q_t if want_qt else None), int(saturate), _stream(stream)),
+        "fp8_quantize_tensor_current")
+    return (q if want_q else None), (q_t if want_qt else None), amax, scale
 
 
 class History:

@@ -228,6 +228,39 @@ int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows, int64_t cols,
   return from_cuda(launch_quant2d(p, stream));
 }
 
+int fp8_quantize_tensor_current(const void *x, int in_dtype, int64_t rows, int64_t cols,
+                                int format, float *amax_out, float *scale_out, uint8_t *q,
+                                uint8_t *q_t, int saturate, cudaStream_t stream) {
+  int rc = check_quant(x, in_dtype, rows, cols, format, q_t != nullptr);
+  if (rc != FP8Q_OK) return rc;
+  if (amax_out == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(amax_out) & 3u) return FP8Q_ERR_MISALIGNED;
+  if (rows > 0 && cols > 0 && q == nullptr && q_t == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK) return rc;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  const int64_t bytes = rows * cols * (in_dtype == FP8Q_DT_BF16 ? 2 : 4);
+  if (rows == 0 || cols == 0 || bytes > kFusedTensorMaxBytes) {
+    if ((rc = fp8_amax(x, in_dtype, rows * cols, amax_out, stream)) != FP8Q_OK) return rc;
+    return fp8_quantize_tensor(x, in_dtype, rows, cols, format, amax_out, scale_out, q, q_t,
+                               saturate, stream);
+  }
+  if (cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = saturate;
+  p.mode = kModeTensorFused;
+  p.err = device_error_word();
+  p.amax_out = amax_out;
+  p.scale_out = scale_out;
+  p.q = q;
+  p.q_t = q_t;
+  return from_cuda(launch_quant2d(p, stream));
+}
+
 int fp8_quantize_delayed(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
                          fp8q_amax_history *hist, float *scale_out, uint8_t *q, uint8_t *q_t,
                          int saturate, cudaStream_t stream) {

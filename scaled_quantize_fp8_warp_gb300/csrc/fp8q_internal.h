@@ -31,7 +31,8 @@ enum QuantMode : int {
   kModeTile = 2,           // 1x128 row tiles and/or 128x1 column tiles
   kModeBlock = 3,          // 128x128 blocks
   kModeRowAmax = 4,        // row-wise pass 1: per-row / per-column amax into the scale arrays
-  kModeRowCast = 5         // row-wise pass 2: cast with per-row / per-column scales
+  kModeRowCast = 5,        // row-wise pass 2: cast with per-row / per-column scales
+  kModeTensorFused = 6     // amax and per-tensor cast in one cooperative launch
 };
 
 struct QuantParams {
@@ -44,6 +45,7 @@ struct QuantParams {
   const float *amax_in;        // kModeTensorCurrent
   fp8q_amax_history *hist;     // kModeTensorDelayed
   float *scale_out;            // tensor modes, nullable
+  float *amax_out;             // kModeTensorFused: max |x| (zero on entry)
   uint8_t *q;                  // [rows, cols] or null
   uint8_t *q_t;                // [cols, rows] or null
   float *q_scales;             // tile: [ceil(cols/128), rows]; block: [nrb, ncb]
@@ -56,6 +58,9 @@ struct QuantParams {
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
                         cudaStream_t stream);
 cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream);
+// Largest input (bytes) quantised by kModeTensorFused: it must stay in L2
+// between the amax pass and the cast.
+constexpr int64_t kFusedTensorMaxBytes = 80ll << 20;
 // Row-wise pass 3: s[i] = max(fl32(s[i] / fmax), 1e-12) in place.
 cudaError_t launch_amax_to_scale(float *s, int64_t n, int format, cudaStream_t stream);
 

@@ -305,7 +305,9 @@ enum KernelMode : int {
   kKBlock = 5,      // 128x128 blocks -> q and/or q_t, block scales
   kKRowAmax = 6,    // row-wise pass 1: per-row / per-column amax, atomicMax into
                     // q_scales / qt_scales (as fp32 bit patterns)
-  kKRowCast = 7     // row-wise pass 2: cast with the scales of those amaxes
+  kKRowCast = 7,    // row-wise pass 2: cast with the scales of those amaxes
+  kKTensorFused = 8 // per-tensor current scaling in one cooperative launch:
+                    // amax over every tile, a grid barrier, then the cast
 };
 
 // Dynamic tile scheduling: each launch of the quantize kernel takes one slot
@@ -334,7 +336,8 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   constexpr bool kRowTiles = (KM == kKTileRow || KM == kKTileBoth);
   constexpr bool kColTiles = (KM == kKTileCol || KM == kKTileBoth);
   constexpr bool kRowwise = (KM == kKRowAmax || KM == kKRowCast);
-  constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock);
+  constexpr bool kFused = (KM == kKTensorFused);
+  constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock || kFused);
   using Ring = QuantRing<InT>;
   const float fm = FmtTraits<FMT>::kMax;
 
@@ -346,6 +349,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   __shared__ __align__(8) uint64_t sh_full[Ring::kStages];
   __shared__ int sh_tr[Ring::kStages], sh_tc[Ring::kStages];  // tile of a stage; -1: none
   __shared__ int sh_abort;
+  __shared__ uint32_t sh_amax_bits;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rg = warp * 2 + (lane >> 4);
@@ -375,6 +379,16 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   // work.  One CTA's tile numbers only grow (one thread's claims on one
   // address come back in increasing order), so after a -1 every later step
   // is -1 as well.
+  // Fused per-tensor mode: a CTA's T tiles are blockIdx.x + j * gridDim.x;
+  // steps 0..T-1 take the amax over them, steps T..2T-1 cast them in reverse
+  // order (the most recently read, likeliest still in L2, first).
+  const int64_t my_tiles =
+      (blockIdx.x < ntiles) ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto fused_tile = [&](int64_t i) -> int64_t {
+    if (i < my_tiles) return (int64_t)blockIdx.x + i * gridDim.x;
+    if (i < 2 * my_tiles) return (int64_t)blockIdx.x + (2 * my_tiles - 1 - i) * gridDim.x;
+    return ntiles;
+  };
   auto issue_tile = [&](int64_t i, int64_t c) {
     const int s = (int)(i % Ring::kStages);
     const uint32_t bar = ptx::smem_u32(&sh_full[s]);
@@ -400,7 +414,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     ptx::prefetch_tmap(&tmx);
 #pragma unroll
     for (int j = 0; j < Ring::kStages; ++j)
-      issue_tile(j, (int64_t)blockIdx.x + (int64_t)j * gridDim.x);
+      issue_tile(j, kFused ? fused_tile(j) : (int64_t)blockIdx.x + (int64_t)j * gridDim.x);
     if (p.dynamic) next_claim = atomicAdd(&work[0], 1u);
   }
   __syncthreads();
@@ -448,13 +462,46 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     const bool all_ok = __syncthreads_and(ok ? 1 : 0) != 0;
     if (!all_ok || tr < 0) break;
     if (tid == 0 && !*abort_flag) {
-      if (p.dynamic) {
+      if (kFused) {
+        issue_tile(i + Ring::kStages, fused_tile(i + Ring::kStages));
+      } else if (p.dynamic) {
         issue_tile(i + Ring::kStages, (int64_t)Ring::kStages * gridDim.x + next_claim);
         next_claim = atomicAdd(&work[0], 1u);
       } else {
         issue_tile(i + Ring::kStages, (int64_t)blockIdx.x + (i + Ring::kStages) * gridDim.x);
       }
       issued = i + Ring::kStages + 1;
+    }
+
+    if (kFused && i == my_tiles) {
+      // Every CTA has taken the amax of its tiles: publish, wait for all the
+      // others (bounded), then every CTA reads the tensor's amax.
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, run_max);
+      if (lane == 0) sh_red[warp] = m;
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t cm = sh_red[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) cm = max(cm, sh_red[w]);
+        unsigned int *amax_bits = reinterpret_cast<unsigned int *>(p.amax_out);
+        if (cm != 0) atomicMax(amax_bits, cm);
+        __threadfence();
+        atomicAdd(&work[0], 1u);
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (*reinterpret_cast<volatile unsigned int *>(&work[0]) < gridDim.x) {
+          if (ptx::globaltimer_ns() - t0 > ptx::kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(p.err, 1u);
+            break;
+          }
+          __nanosleep(64);
+        }
+        __threadfence();
+        sh_amax_bits = *reinterpret_cast<volatile unsigned int *>(amax_bits);
+      }
+      __syncthreads();
+      s_u = scale_from_amax(__uint_as_float(sh_amax_bits), fm);
+      r_u = __fdiv_rn(1.0f, s_u);
     }
 
     uint32_t rowmax[8];
@@ -476,7 +523,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     }
 
     // ------------------------------------------------ uniform-scale modes
-    if (kUniform) {
+    if (kFused && i < my_tiles) {
+      run_max = max(run_max, tmax);   // amax pass: nothing is stored
+    } else if (kUniform) {
       float s = s_u, r = r_u;
       if (KM == kKBlock) {
         uint32_t m = __reduce_max_sync(0xFFFFFFFFu, tmax);
@@ -677,7 +726,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
     // Shared scratch that crosses warps is reused by the next tile.  Per-tensor,
     // delayed and 1x128 row-tile casts keep theirs per warp (ordered by the
     // barrier at the top of the next iteration).
-    if (!(KM == kKTensor || KM == kKDelayed || KM == kKTileRow)) __syncthreads();
+    if (!(KM == kKTensor || KM == kKDelayed || KM == kKTileRow || kFused)) __syncthreads();
   }
 
   if (tid == 0) {
@@ -692,8 +741,9 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
       }
     }
     // Every claim of this CTA precedes its "done"; the last CTA resets the slot.
-    if (p.dynamic) __threadfence();
-    if (p.dynamic && atomicAdd(&work[1], 1u) == gridDim.x - 1) {
+    const bool uses_slot = p.dynamic || kFused;
+    if (uses_slot) __threadfence();
+    if (uses_slot && atomicAdd(&work[1], 1u) == gridDim.x - 1) {
       work[0] = 0u;
       work[1] = 0u;
       __threadfence();
@@ -701,7 +751,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2)
   }
 
   // ------------------------------------------ per-tensor scale bookkeeping
-  if (KM == kKTensor) {
+  if (KM == kKTensor || kFused) {
     if (blockIdx.x == 0 && tid == 0 && p.scale_out != nullptr) *p.scale_out = s_u;
   }
   if (KM == kKDelayed) {
@@ -821,8 +871,26 @@ cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
   if (grid < 1) grid = 1;
   static std::atomic<unsigned int> next_slot{0};
   QuantParams q = p;
-  q.dynamic = ntiles >= 8 * grid ? 1 : 0;
-  q.work_slot = q.dynamic ? (int)(next_slot.fetch_add(1u) % kQuantWorkSlots) : 0;
+  q.dynamic = (KM != kKTensorFused && ntiles >= 8 * grid) ? 1 : 0;
+  q.work_slot = (q.dynamic || KM == kKTensorFused)
+                    ? (int)(next_slot.fetch_add(1u) % kQuantWorkSlots)
+                    : 0;
+  if (KM == kKTensorFused) {
+    // every CTA must be resident for the grid barrier: a cooperative launch
+    // guarantees it (or fails)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
+    cfg.dynamicSmemBytes = Ring::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmx, q);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   kernel<<<(unsigned)grid, kQuantThreads, Ring::kSmemBytes, stream>>>(tmx, q);
   return cudaGetLastError();
 }
@@ -840,6 +908,8 @@ cudaError_t dispatch_mode(const QuantParams &p, cudaStream_t stream) {
       return launch_variant<InT, FMT, kKRowAmax>(p, stream);
     case kModeRowCast:
       return launch_variant<InT, FMT, kKRowCast>(p, stream);
+    case kModeTensorFused:
+      return launch_variant<InT, FMT, kKTensorFused>(p, stream);
     case kModeTile:
       if (p.q != nullptr && p.q_t != nullptr) return launch_variant<InT, FMT, kKTileBoth>(p, stream);
       if (p.q != nullptr) return launch_variant<InT, FMT, kKTileRow>(p, stream);

@@ -119,6 +119,13 @@ def test_validation_before_device(lib):
     bad = fq.Operand(0x10000, fq.E4M3, 9, 0x20000, 0, 0)
     assert lib.fp8_gemm(ctypes.byref(bad), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32, 32,
                         None) == 1
+    # quantize with its own amax: the amax output is required and 4-byte aligned
+    assert lib.fp8_quantize_tensor_current(aligned, fq.DT_BF16, 16, 32, fq.E4M3, None, None,
+                                           aligned, None, 0, None) == 1
+    assert lib.fp8_quantize_tensor_current(aligned, fq.DT_BF16, 16, 32, fq.E4M3, P(0x10002),
+                                           None, aligned, None, 0, None) == 2
+    assert lib.fp8_quantize_tensor_current(aligned, fq.DT_BF16, 16, 24, fq.E4M3, aligned, None,
+                                           aligned, None, 0, None) == 1
     # gemm with fused amax: needs a 4-byte aligned amax, then validates as fp8_gemm
     assert lib.fp8_gemm_amax(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32,
                              32, None, None) == 1

@@ -281,3 +281,61 @@ def test_rowwise_repeated_calls_reset_accumulators(fq):
     assert_f32_bits_equal(f32(qts), rqts, "column scales")
     assert_bytes_equal(u8(q), rq, "row bytes")
     assert_bytes_equal(u8(qt), rqt, "column bytes")
+
+
+# ------------------------------------------- amax + cast in one call
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape,which", [
+    ((128, 128), "q"), ((200, 176), "q"), ((1024, 272), "both"), ((272, 48), "qt"),
+    ((8192, 4096), "both"),        # the activation: one cooperative launch
+    ((12288, 4096), "both"),       # 96 MiB of bf16: above the L2 limit, two kernels
+])
+def test_quantize_tensor_current_matches_two_calls(fq, dtype, shape, which):
+    """fp8_quantize_tensor_current equals fp8_amax + fp8_quantize_tensor bit
+    for bit (amax, scale, q, q_t) and the oracle's per-tensor quantisation."""
+    x, _ = workloads.with_outlier_rows(shape, 1.0, 0.02, 300.0, 44, dtype=dtype)
+    xd = x.cuda()
+    want_q, want_qt = which in ("q", "both"), which in ("qt", "both")
+    q, qt, am, sc = fq.fp8_quantize_tensor_current(xd, 0, want_q=want_q, want_qt=want_qt)
+    am2 = fq.fp8_amax(xd)
+    q2, qt2, sc2 = fq.fp8_quantize_tensor(xd, 0, am2, want_q=want_q, want_qt=want_qt)
+    assert fq.device_status() == 0
+    assert_f32_bits_equal(f32(am), f32(am2), "amax")
+    assert_f32_bits_equal(f32(sc), f32(sc2), "scale")
+    if want_q:
+        assert_bytes_equal(u8(q), u8(q2), "q")
+    if want_qt:
+        assert_bytes_equal(u8(qt), u8(qt2), "q_t")
+    if shape[0] * shape[1] <= 1 << 20:
+        rq, rqt, rs = oracle.quantize_tensor(to_oracle(x), 0, want_q=want_q, want_qt=want_qt)
+        assert_f32_bits_equal(f32(sc), np.array([rs], np.float32), "oracle scale")
+        if want_q:
+            assert_bytes_equal(u8(q), rq, "oracle q")
+
+
+def test_quantize_tensor_current_special_values_and_repeats(fq):
+    """NaN / Inf propagate as in the two-call path; repeated calls with the
+    same outputs start from a zeroed amax."""
+    x = workloads.normal((256, 512), 1.0, 45)
+    for case in ("plain", "inf", "nan", "plain"):
+        y = x.clone()
+        if case == "inf":
+            y[3, 7] = float("inf")
+        if case == "nan":
+            y[100, 200] = float("nan")
+        yd = y.cuda()
+        q, _, am, sc = fq.fp8_quantize_tensor_current(yd, 1)
+        am2 = fq.fp8_amax(yd)
+        q2, _, sc2 = fq.fp8_quantize_tensor(yd, 1, am2)
+        assert fq.device_status() == 0
+        assert_f32_bits_equal(f32(am), f32(am2), case + " amax")
+        assert_f32_bits_equal(f32(sc), f32(sc2), case + " scale")
+        assert_bytes_equal(u8(q), u8(q2), case + " q")
+
+
+def test_quantize_tensor_current_empty(fq):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    q, _, am, sc = fq.fp8_quantize_tensor_current(x, 0)
+    assert fq.device_status() == 0
+    assert f32(am)[0] == 0.0

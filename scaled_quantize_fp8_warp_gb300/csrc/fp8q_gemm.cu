@@ -68,7 +68,10 @@ static_assert(kTensorCM == 1 || kTensorCM == 2 || kTensorCM == 4, "cluster of 1,
 // kPairAcc TMEM accumulators of 256 columns each.
 constexpr bool kTensorPair = FP8Q_TENSOR_PAIR != 0;
 constexpr int kPairAcc = FP8Q_PAIR_ACC;
-constexpr int kPairStages = 6;
+#ifndef FP8Q_PAIR_STAGES
+#define FP8Q_PAIR_STAGES 6
+#endif
+constexpr int kPairStages = FP8Q_PAIR_STAGES;   // 32 KB ring stages of the pair kernel
 constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
 constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 

@@ -330,15 +330,31 @@ struct QuantRing {
   static constexpr int kSmemBytes = kStages * kTileBytes + 1024;  // + alignment slack
 };
 
+#ifndef FP8Q_QUANT_MINB3
+#define FP8Q_QUANT_MINB3 1
+#endif
+// CTAs per SM a mode is built for: the lighter casts can run three CTAs of
+// two-stage rings (the same tiles in flight per SM, 50% more warps to hide the
+// cast's latency); the heavier ones keep two CTAs of three stages.
+template <typename InT, int KM>
+struct QuantShape {
+  static constexpr bool kThree = FP8Q_QUANT_MINB3 != 0 && sizeof(InT) == 2 &&
+                                 (KM == 0 || KM == 1 || KM == 2 || KM == 5 || KM == 6 || KM == 8);
+  static constexpr int kMinBlocks = kThree ? 3 : 2;
+  static constexpr int kStages = kThree ? 2 : QuantRing<InT>::kStages;
+  static constexpr int kTileBytes = QuantRing<InT>::kTileBytes;
+  static constexpr int kSmemBytes = kStages * kTileBytes + 1024;
+};
+
 template <typename InT, int FMT, int KM>
-__global__ void __launch_bounds__(kQuantThreads, 2)
+__global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlocks))
     quant2d_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr bool kRowTiles = (KM == kKTileRow || KM == kKTileBoth);
   constexpr bool kColTiles = (KM == kKTileCol || KM == kKTileBoth);
   constexpr bool kRowwise = (KM == kKRowAmax || KM == kKRowCast);
   constexpr bool kFused = (KM == kKTensorFused);
   constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock || kFused);
-  using Ring = QuantRing<InT>;
+  using Ring = QuantShape<InT, KM>;
   const float fm = FmtTraits<FMT>::kMax;
 
   extern __shared__ uint8_t dyn_smem[];
@@ -840,7 +856,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
 
 template <typename InT, int FMT, int KM>
 cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
-  using Ring = QuantRing<InT>;
+  using Ring = QuantShape<InT, KM>;
   auto kernel = quant2d_kernel<InT, FMT, KM>;
   static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {

@@ -824,10 +824,17 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
       m = max(m, w.w & 0x7FFFFFFFu);
     }
   };
-  for (; i + 3 * stride < nvec; i += 4 * stride) {
-    uint4 w0 = __ldg(xv + i), w1 = __ldg(xv + i + stride), w2 = __ldg(xv + i + 2 * stride),
-          w3 = __ldg(xv + i + 3 * stride);
-    upd(w0); upd(w1); upd(w2); upd(w3);
+#ifndef FP8Q_AMAX_UNROLL
+#define FP8Q_AMAX_UNROLL 8
+#endif
+  // FP8Q_AMAX_UNROLL 16-byte loads in flight per thread per round trip
+  constexpr int U = FP8Q_AMAX_UNROLL;
+  for (; i + (U - 1) * stride < nvec; i += U * stride) {
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) w[u] = __ldg(xv + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < U; ++u) upd(w[u]);
   }
   for (; i < nvec; i += stride) upd(__ldg(xv + i));
   if (sizeof(InT) == 2) m = max(m & 0xFFFFu, m >> 16) << 16;

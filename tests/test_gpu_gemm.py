@@ -232,6 +232,41 @@ def test_layer_fprop_full_size_tensor(fq, layer):
     check_bound(f32(y)[ms, ns], yr, ab, True, f"{shape.name} fprop")
 
 
+@pytest.mark.parametrize("layer", [2, 3])      # MLP up, MLP down: the largest shapes
+def test_layer_all_roles_full_size_tensor(fq, layer):
+    """Per-tensor current scaling of x, w and grad_out with both orientations
+    (bit-exact against the oracle), then Fprop, Dgrad and Wgrad on sampled
+    outputs, at the layer's full size: tensors of 15872 x 16384 and
+    contractions over 16384, on the paths the layer step times (dynamic tile
+    claiming, CTA-pair GEMM)."""
+    shape = workloads.LAYER[layer]
+    x, w, g = workloads.layer_inputs(shape, layer)
+    M, K, N = x.shape[0], shape.K, shape.N
+    q, ref = {}, {}
+    for nm, t, fmt in (("x", x, 0), ("w", w, 0), ("g", g, 1)):
+        td = t.cuda()
+        q[nm] = fq.fp8_quantize_tensor(td, fmt, fq.fp8_amax(td), want_q=True, want_qt=True)
+        del td
+        ref[nm] = oracle.quantize_tensor(to_oracle(t), fmt, want_q=True, want_qt=True)
+        assert_bytes_equal(u8(q[nm][0]), ref[nm][0], nm)
+        assert_bytes_equal(u8(q[nm][1]), ref[nm][1], nm + "_t")
+        assert_f32_bits_equal(f32(q[nm][2]), np.array([ref[nm][2]], np.float32), nm + " scale")
+    T, RT = fq.GemmOperand.tensor, oracle.GemmOperand.tensor
+    y = fq.fp8_gemm_fprop(T(q["x"][0], 0, q["x"][2]), T(q["w"][0], 0, q["w"][2]))
+    dx = fq.fp8_gemm_dgrad(T(q["g"][0], 1, q["g"][2]), T(q["w"][1], 0, q["w"][2]))
+    dw = fq.fp8_gemm_wgrad(T(q["g"][1], 1, q["g"][2]), T(q["x"][1], 0, q["x"][2]))
+    gpu_status_ok(fq)
+    rng = np.random.default_rng(10 + layer)
+    for got, opA, opB, Rr, Cc, nm in [
+        (y, RT(ref["x"][0], 0, ref["x"][2]), RT(ref["w"][0], 0, ref["w"][2]), M, N, "fprop"),
+        (dx, RT(ref["g"][0], 1, ref["g"][2]), RT(ref["w"][1], 0, ref["w"][2]), M, K, "dgrad"),
+        (dw, RT(ref["g"][1], 1, ref["g"][2]), RT(ref["x"][1], 0, ref["x"][2]), N, K, "wgrad"),
+    ]:
+        ms, ns = _sample_points(Rr, Cc, rng, n=2048)
+        yr, ab = oracle.gemm_points(opA, opB, ms, ns)
+        check_bound(f32(got)[ms, ns], yr, ab, True, f"{shape.name} {nm}")
+
+
 def test_layer_all_roles_full_size_block(fq):
     """Attention-out layer at full size with 1x128 / 128x128 scaling: fprop,
     dgrad (B = w^T, transposed block scales) and wgrad (column tiles of g and

@@ -336,14 +336,21 @@ struct QuantRing {
 // CTAs per SM a mode is built for: bf16 input runs three CTAs of two-stage
 // rings (the same tiles in flight per SM as two CTAs of three stages, with 50%
 // more warps to hide the cast's latency; every mode fits 85 registers without
-// spills); fp32 input keeps its two-stage ring of 64 KB tiles.
+// spills), except the column-tile modes, whose scratch plus the 8 KB
+// transposed-copy staging leave room for two CTAs of three stages; fp32 input
+// keeps its two-stage ring of 64 KB tiles.
 template <typename InT, int KM>
 struct QuantShape {
-  static constexpr bool kThree = FP8Q_QUANT_MINB3 != 0 && sizeof(InT) == 2;
+  // modes that can write the transposed copy stage it through shared memory
+  static constexpr bool kStaging = !(KM == 2 || KM == 6);
+  static constexpr int kStageBytes = kStaging ? 64 * 128 : 0;
+  // the column-tile modes' own scratch would not leave room for three
+  static constexpr bool kThree = FP8Q_QUANT_MINB3 != 0 && sizeof(InT) == 2 &&
+                                 !(KM == 3 || KM == 4 || KM == 7);
   static constexpr int kMinBlocks = kThree ? 3 : 2;
   static constexpr int kStages = kThree ? 2 : QuantRing<InT>::kStages;
   static constexpr int kTileBytes = QuantRing<InT>::kTileBytes;
-  static constexpr int kSmemBytes = kStages * kTileBytes + 1024;
+  static constexpr int kSmemBytes = kStages * kTileBytes + kStageBytes + 1024;
 };
 
 template <typename InT, int FMT, int KM>
@@ -377,7 +384,41 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
   const uint32_t raw = ptx::smem_u32(dyn_smem);
   const uint32_t ring = (raw + 1023u) & ~1023u;
   const uint8_t *ring_ptr = dyn_smem + (ring - raw);
+  uint8_t *qt_stage = dyn_smem + (ring - raw) + Ring::kStages * Ring::kTileBytes;
   volatile int *abort_flag = &sh_abort;
+
+  // The transposed FP8 tile (q_t rows c0.., byte columns r0..) goes out as
+  // whole 128-byte rows: each thread's 8 x 8 bytes (cb[j] = q_t row
+  // cbase + j, bytes rbase..rbase+7) are staged in shared memory, 64 q_t rows
+  // at a time, then 8 consecutive threads write one row.  The 16-byte chunk
+  // of a row is XOR-swizzled by its 8-row group so that the staging writes of
+  // a warp hit distinct banks.  Every thread of the CTA must call this.
+  auto store_qt = [&](const uint2 (&cb)[8], bool valid, int64_t r0, int64_t c0) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      if (valid && (cg >> 3) == half) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int row = (cg & 7) * 8 + j;
+          const int chunk = (rg >> 1) ^ (cg & 7);
+          *reinterpret_cast<uint2 *>(qt_stage + row * 128 + chunk * 16 + (rg & 1) * 8) = cb[j];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int c = tid + k * kQuantThreads;
+        const int row = c >> 3, chunk = c & 7;
+        const int64_t qrow = c0 + half * 64 + row;   // input column
+        const int64_t qcol = r0 + chunk * 16;          // input row (rows % 16 == 0)
+        if (qrow < cols && qcol < rows)
+          *reinterpret_cast<uint4 *>(p.q_t + qrow * rows + qcol) =
+              *reinterpret_cast<const uint4 *>(qt_stage + row * 128 +
+                                               (chunk ^ ((row >> 3) & 7)) * 16);
+      }
+      __syncthreads();
+    }
+  };
 
   // Per-tensor current scaling runs right after the amax pass over the same
   // data, so it hands out the tiles backwards and meets the most recently read
@@ -565,12 +606,10 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
           if (rbase + i < rows)
             *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = rb[i];
       }
-      if (p.q_t != nullptr && col_ok && rchunk_ok) {
+      if (p.q_t != nullptr) {
         uint2 cb[8];
         transpose8x8(rb, cb);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = cb[j];
+        store_qt(cb, col_ok && rchunk_ok, r0, c0);
       }
     }
 
@@ -640,17 +679,19 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
         if (c0 + tid < cols) p.qt_scales[tr * cols + c0 + tid] = s;
       }
       __syncthreads();
-      if (col_ok && rchunk_ok) {
+      uint2 cb[8];
+      const bool valid = col_ok && rchunk_ok;
+      if (valid) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float s = sh_col_s[cg * 8 + j], r = sh_col_r[cg * 8 + j];
           float cv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
-          uint2 b = cast8<FMT>(cv, s, r, fast_ok<FMT>(colmax[j], r), saturate);
-          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = b;
+          cb[j] = cast8<FMT>(cv, s, r, fast_ok<FMT>(colmax[j], r), saturate);
         }
       }
+      store_qt(cb, valid, r0, c0);
     }
     // ------------------------------------------- row-wise scaling, pass 1
     if (KM == kKRowAmax) {
@@ -726,17 +767,21 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
           if (rbase + i < rows) *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = b;
         }
       }
-      if (p.qt_scales != nullptr && col_ok && rchunk_ok) {
+      if (p.qt_scales != nullptr) {
+        uint2 cb[8];
+        const bool valid = col_ok && rchunk_ok;
+        if (valid) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float sc = sh_col_s[cg * 8 + j], rc = sh_col_r[cg * 8 + j];
-          float cv[8];
+          for (int j = 0; j < 8; ++j) {
+            const float sc = sh_col_s[cg * 8 + j], rc = sh_col_r[cg * 8 + j];
+            float cv[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
-          uint2 b = cast8<FMT>(cv, sc, rc, fast_ok<FMT>(Row8<InT>::colmax_bits(cmp, j), rc),
-                               saturate);
-          *reinterpret_cast<uint2 *>(p.q_t + (cbase + j) * rows + rbase) = b;
+            for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
+            cb[j] = cast8<FMT>(cv, sc, rc,
+                               fast_ok<FMT>(Row8<InT>::colmax_bits(cmp, j), rc), saturate);
+          }
         }
+        store_qt(cb, valid, r0, c0);
       }
     }
     // Shared scratch that crosses warps is reused by the next tile.  Per-tensor,

@@ -872,7 +872,9 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
 #ifndef FP8Q_AMAX_UNROLL
 #define FP8Q_AMAX_UNROLL 8
 #endif
-  // FP8Q_AMAX_UNROLL 16-byte loads in flight per thread per round trip
+  // FP8Q_AMAX_UNROLL 16-byte loads in flight per thread per round trip; the
+  // last round is predicated rather than finished one load at a time, so a
+  // thread never waits out more than one round trip per U loads
   constexpr int U = FP8Q_AMAX_UNROLL;
   for (; i + (U - 1) * stride < nvec; i += U * stride) {
     uint4 w[U];
@@ -881,7 +883,14 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
 #pragma unroll
     for (int u = 0; u < U; ++u) upd(w[u]);
   }
-  for (; i < nvec; i += stride) upd(__ldg(xv + i));
+  if (i < nvec) {
+    uint4 w[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      w[u] = (i + u * stride < nvec) ? __ldg(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) upd(w[u]);
+  }
   if (sizeof(InT) == 2) m = max(m & 0xFFFFu, m >> 16) << 16;
   // scalar tail (fewer than kVec elements)
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

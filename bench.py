@@ -533,6 +533,37 @@ class Runner:
         fin.record(self._cout)
         st.wait_event(fin)
 
+    def link_rates(self, reps: int = 3):
+        """Host<->device copy rates over this step's own pinned buffers: the
+        inputs in alone, the outputs out alone, and both at once (GB/s, median
+        of `reps`, wall clock between device synchronisations).  The
+        both-at-once time is the floor of an end-to-end step."""
+        torch = self.torch
+        ins = [(L[k], L[k + "_h"]) for L in self.s.linears for k in "xwg"]
+        outs = [(L[o + "_h"], L[o]) for L in self.s.linears for o in ("y", "dx", "dw")]
+
+        def issue(pairs, stream):
+            with torch.cuda.stream(stream):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+
+        def timed(fn):
+            ts = []
+            for _ in range(reps):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                ts.append(time.perf_counter() - t0)
+            return statistics.median(ts)
+
+        t_in = timed(lambda: issue(ins, self._cin))
+        t_out = timed(lambda: issue(outs, self._cout))
+        t_both = timed(lambda: (issue(ins, self._cin), issue(outs, self._cout)))
+        hb, db = self.s.h2d_bytes, self.s.d2h_bytes
+        return {"h2d_gbs": hb / t_in / 1e9, "d2h_gbs": db / t_out / 1e9,
+                "both_gbs": (hb + db) / t_both / 1e9, "floor_ms": t_both * 1e3}
+
     def e2e_tensor_serial(self):
         st = self.stream
         with self.torch.cuda.stream(st):
@@ -790,7 +821,9 @@ def main():
         ms_f_fused = time_steps(torch, dist, stream, lambda: fq.fp8_gemm_amax(
             xA, wB, out=y0, amax=am_y, stream=stream), K, W, clk=clk)
 
-    # ---- end to end through host buffers (headline recipe)
+    # ---- end to end through host buffers (headline recipe), with the host
+    # link's own rates over the same buffers just before, since they bound it
+    link = run.link_rates()
     ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), W)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
@@ -983,7 +1016,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": tf(ms_e2e), "unit": "TFLOP/s",
                 "ms_per_step": ms_e2e, "h2d_bytes_per_step": state.h2d_bytes,
-                "d2h_bytes_per_step": state.d2h_bytes},
+                "d2h_bytes_per_step": state.d2h_bytes, "host_link": link},
         "gpu_launches": Runner.tensor_autocast.launches * K,
         "clocks": clk.summary(),
     }

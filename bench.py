@@ -981,14 +981,14 @@ def main():
             "tensor_current": {"GB/s (over 3 B/elem)": gbps(3 * n, ms_tensor),
                                "us": ms_tensor * 1e3,
                                "frac": gbps(3 * n, ms_tensor) / hbm_peak,
-                               "how": ("fp8_quantize_tensor_current: amax pass, grid barrier and "
-                                       "cast from L2 in one cooperative launch"),
+                               "how": ("fp8_quantize_tensor_current: at this size the amax and "
+                                       "cast kernels (one cooperative launch only up to 8 MiB, "
+                                       "where it is the faster)"),
                                "two_kernels_us": ms_tensor_2k * 1e3},
             "both_orientations": {
                 "note": ("q and q_t from one call; GB/s over the unique bytes (2 B read + "
                          "2 B written per element); row-wise and per-tensor read x twice "
-                         "(amax pass, then cast), the second read mostly from L2 (per-tensor: "
-                         "one cooperative launch)"),
+                         "(amax pass, then cast), the second read mostly from L2"),
                 "tile1x128_rows_and_cols": {"GB/s": gbps(dual_bytes, ms_tile2),
                                             "us": ms_tile2 * 1e3,
                                             "frac": gbps(dual_bytes, ms_tile2) / hbm_peak},

@@ -165,10 +165,10 @@ int fp8_quantize_tensor(const void *x, int in_dtype, int64_t rows,
  * then the cast of fp8_quantize_tensor with that amax ([fp8_parity]
  * scaled_roundtrip with scale=None: amax, scale and cast together).  Results
  * are those of fp8_amax followed by fp8_quantize_tensor, bit for bit.
- *   When x holds at most 80 MiB (it then stays in the L2 cache between the
- *   two passes) both run in one cooperative launch: the amax pass reads x,
- *   a grid-wide barrier publishes the amax, and the cast re-reads x from L2.
- *   Larger inputs run the two kernels.
+ *   When x holds at most 8 MiB both run in one cooperative launch: the amax
+ *   pass reads x, a grid-wide barrier publishes the amax, and the cast
+ *   re-reads x from the L2 cache.  Larger inputs run the two kernels, which
+ *   are faster there.
  *   amax_out   device float, 4-byte aligned: receives max |x| (zeroed on
  *              `stream` first)
  *   the other arguments as fp8_quantize_tensor.

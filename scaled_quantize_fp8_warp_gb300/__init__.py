@@ -199,7 +199,7 @@ def fp8_quantize_tensor(x, fmt, amax, want_q=True, want_qt=False, saturate=False
 def fp8_quantize_tensor_current(x, fmt, want_q=True, want_qt=False, saturate=False, q=None,
                                 q_t=None, amax=None, scale=None, stream=None):
     """amax and per-tensor cast in one call (one cooperative launch when x
-    fits in L2).  Returns (q | None, q_t | None, amax [1], scale [1])."""
+    holds at most 8 MiB).  Returns (q | None, q_t | None, amax [1], scale [1])."""
     R, C = _rows_cols(x)
     if want_q and q is None:
         q = _empty((R, C), torch.uint8, x)

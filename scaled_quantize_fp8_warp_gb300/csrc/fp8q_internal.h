@@ -58,9 +58,11 @@ struct QuantParams {
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
                         cudaStream_t stream);
 cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream);
-// Largest input (bytes) quantised by kModeTensorFused: it must stay in L2
-// between the amax pass and the cast.
-constexpr int64_t kFusedTensorMaxBytes = 80ll << 20;
+// Largest input (bytes) quantised by kModeTensorFused.  Up to here the one
+// launch saves more than its grid barrier costs (4 and 8 MiB: 0.2-2 us
+// faster); from 16 MiB the amax and cast kernels are 1.6-5 us faster, and the
+// input must in any case stay in L2 between the two passes.
+constexpr int64_t kFusedTensorMaxBytes = 8ll << 20;
 // Row-wise pass 3: s[i] = max(fl32(s[i] / fmax), 1e-12) in place.
 cudaError_t launch_amax_to_scale(float *s, int64_t n, int format, cudaStream_t stream);
 

@@ -288,8 +288,8 @@ def test_rowwise_repeated_calls_reset_accumulators(fq):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("shape,which", [
     ((128, 128), "q"), ((200, 176), "q"), ((1024, 272), "both"), ((272, 48), "qt"),
-    ((8192, 4096), "both"),        # the activation: one cooperative launch
-    ((12288, 4096), "both"),       # 96 MiB of bf16: above the L2 limit, two kernels
+    ((2048, 2048), "both"),        # 8 MiB of bf16: one cooperative launch (fp32: two kernels)
+    ((8192, 4096), "both"),        # the activation, 64 MiB: two kernels
 ])
 def test_quantize_tensor_current_matches_two_calls(fq, dtype, shape, which):
     """fp8_quantize_tensor_current equals fp8_amax + fp8_quantize_tensor bit

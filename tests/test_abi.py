@@ -34,7 +34,7 @@ def header_functions():
                                  text, flags=re.M)))
 
 
-def test_header_declares_the_surveyed_calls():
+def test_header_declares_the_layer_entry_points():
     fns = header_functions()
     for name in ("fp8_amax", "fp8_quantize_tensor", "fp8_quantize_tile1x128",
                  "fp8_quantize_delayed", "fp8_gemm_fprop", "fp8_gemm_dgrad", "fp8_gemm_wgrad",

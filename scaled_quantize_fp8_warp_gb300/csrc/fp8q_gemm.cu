@@ -2,17 +2,21 @@
 // ("fp8_parity.py", FP8Matmul: xq @ wq.T; the blog repost's Fprop / Dgrad /
 // Wgrad shapes), on the 5th-generation tensor cores.
 //
-// Both kernels are persistent (one CTA per SM, static round-robin over output
-// tiles grouped 16 M-tiles at a time for L2 reuse) and warp-specialised:
-//   warp 0   TMA producer: 128x128-byte A and BNx128-byte B boxes, 128-byte
-//            swizzle, into a STAGES-deep shared-memory ring (full/empty
-//            mbarriers);
-//   warp 1   allocates TMEM and issues tcgen05.mma.kind::f8f6f4 (M = 128,
-//            N = BN, K = 32 per instruction, four per 128-byte K block) from
-//            one thread; tcgen05.commit releases ring slots and hands
-//            accumulators on;
-//   warps 2+ epilogue (per-tensor kernel) or promotion + epilogue (block
-//            kernel): tcgen05.ld from TMEM, scale, convert, store.
+// Three persistent, warp-specialised kernels (static round-robin over output
+// tiles, grouped along M for L2 reuse):
+//   gemm_tensor_pair_kernel  per-tensor / row scales at N > 128: a CTA pair
+//            (cta_group::2) computes 256 x 256 tiles, each CTA staging its own
+//            128 rows of A and of B;
+//   gemm_tensor_kernel       per-tensor / row scales at N <= 128, one SM per
+//            128 x BN tile (BN = 64 or 128);
+//   gemm_blockscaled_kernel  1x128 / 128x128 scales, one SM per 128 x 256 tile.
+// Roles: warp 0 is the TMA producer (128-byte swizzled boxes into a
+// shared-memory ring with full/empty mbarriers); warp 1 allocates TMEM and
+// issues tcgen05.mma.kind::f8f6f4 (K = 32 per instruction, four per 128-byte
+// K block) from one thread, with tcgen05.commit releasing ring slots and
+// handing accumulators on; the remaining warps drain TMEM (tcgen05.ld),
+// scale, convert and store.  Every TMA load fetches into the issuing CTA's
+// own shared memory.
 // Per-tensor scaling accumulates the whole K range in TMEM (two accumulator
 // buffers so one tile's epilogue overlaps the next tile's MMAs) and applies
 // s_A s_B once.  Tile/block scaling accumulates each 128-wide K block into a
@@ -46,32 +50,11 @@ constexpr int kGroupM = 16;         // M-tiles per raster group
 #define FP8Q_BLOCK_BN 256
 #define FP8Q_BLOCK_WG 2
 #endif
-#ifndef FP8Q_TENSOR_BK
-#define FP8Q_TENSOR_BK 128
-#endif
-#ifndef FP8Q_TENSOR_CM
-#define FP8Q_TENSOR_CM 2
-#endif
-// K-block width of the per-tensor kernel at BN = 256 (64 -> a deeper ring).
-constexpr int kTensorBK = FP8Q_TENSOR_BK;
-// CTAs per cluster of the per-tensor kernel at BN = 256 (1, 2 or 4): they
-// share B's tile through TMA multicast.
-constexpr int kTensorCM = FP8Q_TENSOR_CM;
-static_assert(kTensorCM == 1 || kTensorCM == 2 || kTensorCM == 4, "cluster of 1, 2 or 4");
-#ifndef FP8Q_TENSOR_PAIR
-#define FP8Q_TENSOR_PAIR 1
-#endif
-#ifndef FP8Q_PAIR_ACC
-#define FP8Q_PAIR_ACC 2
-#endif
-// Per-tensor / row scaling at N > 128 on CTA pairs (cta_group::2) with
-// kPairAcc TMEM accumulators of 256 columns each.
-constexpr bool kTensorPair = FP8Q_TENSOR_PAIR != 0;
-constexpr int kPairAcc = FP8Q_PAIR_ACC;
-#ifndef FP8Q_PAIR_STAGES
-#define FP8Q_PAIR_STAGES 6
-#endif
-constexpr int kPairStages = FP8Q_PAIR_STAGES;   // 32 KB ring stages of the pair kernel
+// Per-tensor / row scaling at N > 128 runs on CTA pairs (cta_group::2) with
+// kPairAcc TMEM accumulators of 256 columns each and a ring of kPairStages
+// 32 KB stages per CTA.
+constexpr int kPairAcc = 2;
+constexpr int kPairStages = 6;
 constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
 constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
 
@@ -102,55 +85,35 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   nt = local / gsize;
 }
 
-// K-block width (bytes = FP8 elements) and its shared-memory swizzle: a
-// 128-byte K block uses 128-byte swizzling (8-row atoms of 1024 bytes), a
-// 64-byte K block 64-byte swizzling (8-row atoms of 512 bytes).
-template <int BK>
-struct Swz;
-template <>
-struct Swz<128> {
-  static constexpr uint32_t kMode = 2;
-  static constexpr uint32_t kSBO = 1024;
-  static constexpr CUtensorMapSwizzle kTma = CU_TENSOR_MAP_SWIZZLE_128B;
-};
-template <>
-struct Swz<64> {
-  static constexpr uint32_t kMode = 4;
-  static constexpr uint32_t kSBO = 512;
-  static constexpr CUtensorMapSwizzle kTma = CU_TENSOR_MAP_SWIZZLE_64B;
-};
+// A 128-byte K block is staged with 128-byte swizzling: 8-row atoms of 1024
+// bytes, shared-memory descriptor swizzle mode 2.
+constexpr uint32_t kSwzMode = 2;
+constexpr uint32_t kSwzSBO = 1024;
 
-template <int BN, int STAGES, int BK = kBK>
+template <int BN, int STAGES>
 struct Layout {
-  static constexpr int kABytes = kBM * BK;
-  static constexpr int kBBytes = BN * BK;
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kRingBytes = STAGES * kStageBytes;
   static constexpr int kBarBytes = 8 * (2 * STAGES + 5);  // full, empty, acc full/empty x2, drain
   static constexpr int kSmemBytes = kRingBytes + kBarBytes + 16 + 1024;  // + align slack
 };
 
-// Producer loop shared by both kernels.  With CM > 1 the CTAs of a cluster
-// work on the CM vertically adjacent tiles (CM u + r, n) of unit u at the same
-// time; they share B's tile, each loading BN / CM of its rows with multicast
-// into every CTA's ring slot, so a slot is refilled only once every CTA's
-// MMAs have released it (its empty barrier counts CM arrivals).
-template <int BN, int STAGES, int BK = kBK, int CM = 1>
+// Producer loop shared by both kernels: one 128 x 128-byte A box and one
+// BN x 128-byte B box per K block, into the next ring slot once the MMAs
+// have released it.
+template <int BN, int STAGES>
 __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUtensorMap *tb,
                                               const GemmArgs &p, uint32_t ring, uint32_t bars,
-                                              volatile int *abort_flag, uint32_t rank = 0) {
-  using L = Layout<BN, STAGES, BK>;
-  constexpr int kPartRows = BN / CM;
-  const int num_mu = (p.num_m_tiles + CM - 1) / CM;
-  const int total = num_mu * p.num_n_tiles;
+                                              volatile int *abort_flag) {
+  using L = Layout<BN, STAGES>;
+  const int total = p.num_m_tiles * p.num_n_tiles;
   uint32_t it = 0;
   bool ok = true;
-  for (int u = blockIdx.x / CM; u < total && ok; u += gridDim.x / CM) {
-    int mu, nt;
-    tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / CM);
-    // a CTA past the last M tile (odd tile count) re-reads that tile's A rows
-    // and stores nothing: it still has to deliver its part of B
-    const int mt = min(mu * CM + (int)rank, p.num_m_tiles - 1);
+  for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+    int mt, nt;
+    tile_coords(u, p.num_m_tiles, p.num_n_tiles, mt, nt);
     for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
       const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
       const uint32_t full = bars + 8 * s, empty = bars + 8 * (STAGES + s);
@@ -160,23 +123,8 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUten
       }
       const uint32_t sa = ring + s * L::kStageBytes;
       mbar_arrive_expect_tx(full, L::kStageBytes);
-      tma_load_2d(sa, ta, kb * BK, mt * kBM, full);
-      if (CM == 1)
-        tma_load_2d(sa + L::kABytes, tb, kb * BK, nt * BN, full);
-      else
-        tma_load_2d_multicast(sa + L::kABytes + rank * (kPartRows * BK), tb, kb * BK,
-                              nt * BN + (int)rank * kPartRows, full, (uint16_t)((1u << CM) - 1));
-    }
-  }
-  if (ok && CM > 1) {
-    // Wait until every CTA has released every slot for the last time: after
-    // this no arrival from another CTA is still on its way to this CTA.
-    for (uint32_t j = 0, jt = it; j < (uint32_t)STAGES; ++j, ++jt) {
-      if (!wait_bounded(bars + 8 * (STAGES + jt % STAGES), ((jt / STAGES) & 1u) ^ 1u,
-                        abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
+      tma_load_2d(sa, ta, kb * kBK, mt * kBM, full);
+      tma_load_2d(sa + L::kABytes, tb, kb * kBK, nt * BN, full);
     }
   }
   if (!ok) {
@@ -193,16 +141,16 @@ __device__ __forceinline__ void producer_loop(const CUtensorMap *ta, const CUten
 }
 
 // MMAs of one K block held in ring slot `s` (BK / 32 MMAs of K = 32).
-template <int BN, int STAGES, int BK = kBK>
+template <int BN, int STAGES>
 __device__ __forceinline__ void issue_kblock(uint32_t ring, uint32_t s, uint32_t d_tmem,
                                              uint32_t idesc, bool accumulate_first) {
-  using L = Layout<BN, STAGES, BK>;
+  using L = Layout<BN, STAGES>;
   const uint32_t a0 = ring + s * L::kStageBytes;
   const uint32_t b0 = a0 + L::kABytes;
 #pragma unroll
-  for (int k = 0; k < BK / kUmmaK; ++k) {
-    const uint64_t ad = sdesc_k(a0 + k * kUmmaK, Swz<BK>::kSBO, Swz<BK>::kMode);
-    const uint64_t bd = sdesc_k(b0 + k * kUmmaK, Swz<BK>::kSBO, Swz<BK>::kMode);
+  for (int k = 0; k < kBK / kUmmaK; ++k) {
+    const uint64_t ad = sdesc_k(a0 + k * kUmmaK, kSwzSBO, kSwzMode);
+    const uint64_t bd = sdesc_k(b0 + k * kUmmaK, kSwzSBO, kSwzMode);
     mma_f8f6f4(d_tmem, ad, bd, idesc, (accumulate_first || k > 0) ? 1u : 0u);
   }
 }
@@ -268,11 +216,11 @@ __device__ __forceinline__ void publish_amax(unsigned int *amax, uint32_t run_ma
 // ------------------------------------------------------------------------
 // Per-tensor scaled GEMM: 6 warps (producer, MMA, 4 epilogue warps).
 // ------------------------------------------------------------------------
-template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC, int CM>
+template <int BN, int STAGES, bool OUT_BF16, bool VEC>
 __global__ void __launch_bounds__(192, 1)
     gemm_tensor_kernel(const __grid_constant__ CUtensorMap ta,
                        const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
-  using L = Layout<BN, STAGES, BK>;
+  using L = Layout<BN, STAGES>;
   constexpr uint32_t kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;  // 128, 256 or 512
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -286,12 +234,10 @@ __global__ void __launch_bounds__(192, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = CM > 1 ? cluster_ctarank() : 0u;
-  constexpr uint16_t kAllCtas = (uint16_t)((1u << CM) - 1);
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, CM);
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf0 + 8 * b, 1);
@@ -310,15 +256,13 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
-  const int num_mu = (p.num_m_tiles + CM - 1) / CM;
-  const int total = num_mu * p.num_n_tiles;
-  const int unit0 = blockIdx.x / CM, unit_step = gridDim.x / CM;
+  const int total = p.num_m_tiles * p.num_n_tiles;
+  const int unit0 = blockIdx.x, unit_step = gridDim.x;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop<BN, STAGES, BK, CM>(&ta, &tb, p, ring, bars, abort_flag, rank);
+    if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
@@ -339,11 +283,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          issue_kblock<BN, STAGES, BK>(ring, s, d_tmem, p.idesc, kb > 0);
-          if (CM == 1)
-            mma_commit(empty0 + 8 * s);
-          else
-            mma_commit_multicast(empty0 + 8 * s, kAllCtas);
+          issue_kblock<BN, STAGES>(ring, s, d_tmem, p.idesc, kb > 0);
+          mma_commit(empty0 + 8 * s);
         }
         if (!ok) break;
         mma_commit(accf0 + 8 * buf);
@@ -359,9 +300,8 @@ __global__ void __launch_bounds__(192, 1)
     const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
     uint32_t acc_it = 0, run_max = 0;
     for (int u = unit0; u < total; u += unit_step, ++acc_it) {
-      int mu, nt;
-      tile_coords(u, num_mu, p.num_n_tiles, mu, nt, kGroupM / CM);
-      const int mt = mu * CM + (int)rank;   // >= num_m_tiles: nothing to store
+      int mt, nt;
+      tile_coords(u, p.num_m_tiles, p.num_n_tiles, mt, nt);
       const uint32_t buf = acc_it & 1u, aph = (acc_it >> 1) & 1u;
       if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
       tc_fence_after();
@@ -398,7 +338,6 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) cluster_sync_all();  // no CTA leaves while another may still signal it
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
@@ -539,8 +478,8 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t a0 = ring + s * L::kStageBytes, b0 = a0 + L::kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint64_t ad = sdesc_k(a0 + k * kUmmaK, Swz<kBK>::kSBO, Swz<kBK>::kMode);
-            const uint64_t bd = sdesc_k(b0 + k * kUmmaK, Swz<kBK>::kSBO, Swz<kBK>::kMode);
+            const uint64_t ad = sdesc_k(a0 + k * kUmmaK, kSwzSBO, kSwzMode);
+            const uint64_t bd = sdesc_k(b0 + k * kUmmaK, kSwzSBO, kSwzMode);
             mma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit_pair_multicast(empty0 + 8 * s, kBoth);
@@ -844,12 +783,11 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
 
 // ------------------------------------------------------------------ host
 
-// Row-major [rows, K] byte matrix, box = box_k x box_rows, 128-byte swizzle,
-// out-of-bounds elements read as zero.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K, uint32_t box_k,
-               uint32_t box_rows) {
-  return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, box_k, box_rows,
-                      box_k == 64 ? Swz<64>::kTma : Swz<128>::kTma);
+// Row-major [rows, K] byte matrix, box = 128 bytes of K x box_rows, 128-byte
+// swizzle, out-of-bounds elements read as zero.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+  return make_tmap_2d(m, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, rows, K, kBK, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <typename KernelT>
@@ -891,44 +829,17 @@ int run_tensor_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
-template <int BN, int STAGES, int BK, bool OUT_BF16, bool VEC, int CM>
+template <int BN, int STAGES, bool OUT_BF16, bool VEC>
 int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                cudaStream_t stream) {
-  using L = Layout<BN, STAGES, BK>;
-  auto kernel = gemm_tensor_kernel<BN, STAGES, BK, OUT_BF16, VEC, CM>;
+  using L = Layout<BN, STAGES>;
+  auto kernel = gemm_tensor_kernel<BN, STAGES, OUT_BF16, VEC>;
   static bool attr_done = false;  // per instantiation
-  static int max_clusters = 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = L::kSmemBytes;
-  cfg.stream = stream;
-  if (CM > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
   if (!attr_done) {
     if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (CM > 1) {
-      // clusters that can be resident at once: a persistent grid larger than
-      // that would leave clusters waiting for others to finish
-      cfg.gridDim = dim3(CM * (sm_count() / CM), 1, 1);
-      if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
-          max_clusters < 1)
-        return FP8Q_ERR_CUDA;
-    }
     attr_done = true;
   }
-  if (CM > 1) {
-    const int units = ((a.num_m_tiles + CM - 1) / CM) * a.num_n_tiles;
-    grid = CM * (units < max_clusters ? units : max_clusters);
-  }
-  cfg.gridDim = dim3(grid, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, a) != cudaSuccess) return FP8Q_ERR_CUDA;
+  kernel<<<grid, 192, L::kSmemBytes, stream>>>(ta, tb, a);
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }
 
@@ -1005,15 +916,11 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   }
   int BN = kBlockScaledBN;
   if (tensor) BN = N <= 64 ? 64 : (N <= 128 ? 128 : 256);
-  // Per-tensor scaling is free to pick its K-block width; tile/block scaling
-  // needs the 128-wide K blocks its scales are defined on.
-  const int BK = (tensor && BN == 256) ? kTensorBK : kBK;
-  // The 256-wide per-tensor kernel runs in clusters of kTensorCM CTAs that
-  // each load BN / kTensorCM rows of B's tile.
-  const int b_box_rows = (tensor && BN == 256) ? BN / (kTensorPair ? 2 : kTensorCM) : BN;
+  // BN = 256 runs on CTA pairs: each CTA loads 128 of the tile's B rows.
+  const int b_box_rows = BN == 256 && tensor ? 128 : BN;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, (uint32_t)BK, kBM) ||
-      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)BK, (uint32_t)b_box_rows))
+  if (!make_tmap(&ta, A.data, (uint64_t)M, (uint64_t)K, kBM) ||
+      !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)b_box_rows))
     return FP8Q_ERR_CUDA;
 
   GemmArgs a{};
@@ -1022,7 +929,7 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   a.K = K;
   a.num_m_tiles = (int)((M + kBM - 1) / kBM);
   a.num_n_tiles = (int)((N + BN - 1) / BN);
-  a.num_k_blocks = (int)((K + BK - 1) / BK);
+  a.num_k_blocks = (int)((K + kBK - 1) / kBK);
   a.idesc = ptx::idesc_f8f6f4((uint32_t)A.format, (uint32_t)B.format, kBM, (uint32_t)BN);
   a.C = C;
   a.scale_a = A.scale;
@@ -1042,33 +949,25 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   if (tiles < grid) grid = (int)tiles;
 
   if (tensor) {
-    constexpr int S256 = kTensorBK == 64 ? 9 : 4;   // ~216 KB or ~192 KB of ring
-    if (kTensorPair && BN == 256 && kTensorBK == 128) {
-      constexpr int PS = kPairStages, PA = kPairAcc;
-      if (vec)
-        return bf16 ? run_tensor_pair<PS, PA, true, true>(ta, tb, a, stream)
-                    : run_tensor_pair<PS, PA, false, true>(ta, tb, a, stream);
-      return bf16 ? run_tensor_pair<PS, PA, true, false>(ta, tb, a, stream)
-                  : run_tensor_pair<PS, PA, false, false>(ta, tb, a, stream);
-    }
+    constexpr int PS = kPairStages, PA = kPairAcc;
     if (vec) {
       if (BN == 64)
-        return bf16 ? run_tensor<64, 8, 128, true, true, 1>(ta, tb, a, grid, stream)
-                    : run_tensor<64, 8, 128, false, true, 1>(ta, tb, a, grid, stream);
+        return bf16 ? run_tensor<64, 8, true, true>(ta, tb, a, grid, stream)
+                    : run_tensor<64, 8, false, true>(ta, tb, a, grid, stream);
       if (BN == 128)
-        return bf16 ? run_tensor<128, 6, 128, true, true, 1>(ta, tb, a, grid, stream)
-                    : run_tensor<128, 6, 128, false, true, 1>(ta, tb, a, grid, stream);
-      return bf16 ? run_tensor<256, S256, kTensorBK, true, true, kTensorCM>(ta, tb, a, grid, stream)
-                  : run_tensor<256, S256, kTensorBK, false, true, kTensorCM>(ta, tb, a, grid, stream);
+        return bf16 ? run_tensor<128, 6, true, true>(ta, tb, a, grid, stream)
+                    : run_tensor<128, 6, false, true>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor_pair<PS, PA, true, true>(ta, tb, a, stream)
+                  : run_tensor_pair<PS, PA, false, true>(ta, tb, a, stream);
     }
     if (BN == 64)
-      return bf16 ? run_tensor<64, 8, 128, true, false, 1>(ta, tb, a, grid, stream)
-                  : run_tensor<64, 8, 128, false, false, 1>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<64, 8, true, false>(ta, tb, a, grid, stream)
+                  : run_tensor<64, 8, false, false>(ta, tb, a, grid, stream);
     if (BN == 128)
-      return bf16 ? run_tensor<128, 6, 128, true, false, 1>(ta, tb, a, grid, stream)
-                  : run_tensor<128, 6, 128, false, false, 1>(ta, tb, a, grid, stream);
-    return bf16 ? run_tensor<256, S256, kTensorBK, true, false, kTensorCM>(ta, tb, a, grid, stream)
-                : run_tensor<256, S256, kTensorBK, false, false, kTensorCM>(ta, tb, a, grid, stream);
+      return bf16 ? run_tensor<128, 6, true, false>(ta, tb, a, grid, stream)
+                  : run_tensor<128, 6, false, false>(ta, tb, a, grid, stream);
+    return bf16 ? run_tensor_pair<PS, PA, true, false>(ta, tb, a, stream)
+                : run_tensor_pair<PS, PA, false, false>(ta, tb, a, stream);
   }
   const bool b_tile = B.scaling == FP8Q_SCALE_TILE_1x128;
   constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;

@@ -71,19 +71,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in `mask` (bit
-// r = cluster rank r): the data lands at offset `dst` of each CTA's shared
-// memory and the bytes are counted on the mbarrier at offset `bar` of each.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *m,
-                                                      int32_t c0, int32_t c1, uint32_t bar,
-                                                      uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-      : "memory");
-}
-
 // Load into this CTA's shared memory, completion counted on an mbarrier that
 // may sit in the peer CTA of the pair (`bar_cluster` is a shared::cluster
 // address, e.g. from mapa).
@@ -219,14 +206,6 @@ __device__ __forceinline__ void mma_commit_pair_multicast(uint32_t bar, uint16_t
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// mma_commit on the mbarrier at offset `bar` of every CTA named in `mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(mask)
       : "memory");
 }
 

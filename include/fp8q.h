@@ -32,9 +32,11 @@
  *     saturate != 0 clamps it to +-fmax.  NaN inputs stay NaN (0x7F | sign).
  *   - Calls are asynchronous on `stream` (0 = legacy default stream).  A
  *     return of FP8Q_OK means the arguments were valid and the work was
- *     enqueued.  Kernels that wait on hardware barriers give up after about a
- *     second and record FP8Q_ERR_TIMEOUT in a device error word that
- *     fp8q_device_status() reports after the stream completes.
+ *     enqueued.  A kernel whose wait on a hardware barrier lasts two seconds
+ *     gives up, records FP8Q_ERR_TIMEOUT in a device error word that
+ *     fp8q_device_status() reports after the stream completes, and returns
+ *     after letting the copies and MMAs it issued finish (each of those
+ *     drains waits at most 0.2 s more).
  *   - The library runs only on compute capability 10.3 (GB300).  Any other
  *     device gives FP8Q_ERR_ARCH; there is no fallback path of any kind.
  *   - Alignment: every device pointer must be 16-byte aligned
@@ -256,7 +258,12 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows,
  *   tile scales of an [R, K] matrix:   stride_row = 1, stride_k = R
  *   block scales of an [R, K] matrix:  stride_row = ceil(K/128), stride_k = 1
  *   block scales used for the transpose [K, R]: stride_row = 1,
- *                                      stride_k = ceil(K/128)  */
+ *                                      stride_k = ceil(K/128)
+ *   row scales:                        stride_row = 1
+ * fp8_gemm and fp8_gemm_amax take any non-negative strides (the caller keeps
+ * every index inside its scale array); the role wrappers fp8_gemm_fprop /
+ * _dgrad / _wgrad accept only the layouts listed here, for the operand's own
+ * shape, and return FP8Q_ERR_INVALID_ARG for any other. */
 typedef struct fp8q_operand {
   const uint8_t *data;
   int32_t format;
@@ -308,7 +315,9 @@ int fp8_gemm_amax(const fp8q_operand *A, const fp8q_operand *B, void *C,
  *   wgrad: dw [N, K] = g^T . x                      (contraction M;
  *          pass g_t [N, M] and x_t [K, M], e.g. column-tile / q_t outputs)
  * Alignment: the contraction and the output column count must be multiples
- * of 16 (so M % 16 == 0 for wgrad).  Errors as fp8_gemm. */
+ * of 16 (so M % 16 == 0 for wgrad).  Each operand's scale strides must be one
+ * of the layouts listed with fp8q_operand for its [rows, contraction] shape.
+ * Errors as fp8_gemm, INVALID_ARG also for a scale layout outside that list. */
 int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y,
                    int out_dtype, int64_t M, int64_t N, int64_t K,
                    cudaStream_t stream);
@@ -322,7 +331,9 @@ int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw,
 /* ----------------------------------------------------- the whole forward */
 
 /* Bytes of workspace fp8_linear_autocast needs for this recipe and shape
- * (rounded up to 256-byte pieces). */
+ * (rounded up to 256-byte pieces); 0 for negative sizes and for sizes whose
+ * element counts M*K or N*K would overflow int64 (which the forward calls
+ * reject with FP8Q_ERR_INVALID_ARG). */
 size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K);
 
 /* Autocast forward of a linear layer ([te_blog] "autocast mode": inputs are

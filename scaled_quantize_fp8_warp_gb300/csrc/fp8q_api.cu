@@ -101,6 +101,32 @@ int check_operand(const fp8q_operand *op, int64_t rows, int64_t K) {
   return FP8Q_OK;
 }
 
+// The role wrappers know every operand's shape, so they accept only the
+// scale layouts the quantize calls write (documented with fp8q_operand): any
+// other stride would index past the scale array on the device.
+//   TILE_1x128 of an [R, K] operand:      stride_row 1, stride_k R
+//   BLOCK_128x128 of an [R, K] operand:   stride_row ceil(K/128), stride_k 1
+//   BLOCK_128x128 read transposed:        stride_row 1, stride_k ceil(R/128)
+//   ROW:                                  stride_row 1
+int check_layout(const fp8q_operand *op, int64_t rows, int64_t K) {
+  const int64_t kb = (K + 127) / 128, rb = (rows + 127) / 128;
+  switch (op->scaling) {
+    case FP8Q_SCALE_TENSOR:
+      return FP8Q_OK;
+    case FP8Q_SCALE_TILE_1x128:
+      return (op->scale_stride_row == 1 && op->scale_stride_k == rows) ? FP8Q_OK
+                                                                       : FP8Q_ERR_INVALID_ARG;
+    case FP8Q_SCALE_BLOCK_128x128:
+      return ((op->scale_stride_row == kb && op->scale_stride_k == 1) ||
+              (op->scale_stride_row == 1 && op->scale_stride_k == rb))
+                 ? FP8Q_OK
+                 : FP8Q_ERR_INVALID_ARG;
+    case FP8Q_SCALE_ROW:
+      return op->scale_stride_row == 1 ? FP8Q_OK : FP8Q_ERR_INVALID_ARG;
+  }
+  return FP8Q_ERR_INVALID_ARG;
+}
+
 GemmOperandDev to_dev(const fp8q_operand *op) {
   GemmOperandDev d;
   d.data = op->data;
@@ -131,6 +157,14 @@ __global__ void selftest_timeout_kernel(unsigned int *err) {
 }
 
 }  // namespace
+
+// Sizes of a linear layer whose element counts M*K and N*K do not overflow.
+bool linear_dims_ok(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return false;
+  const int64_t lim = INT64_MAX / 4;  // room for the byte sums of the workspace
+  if (K > 0 && (M > lim / K || N > lim / K)) return false;
+  return true;
+}
 
 unsigned int *device_error_word() {
   DeviceInfo *d = current_device();
@@ -447,26 +481,41 @@ int fp8_gemm_amax(const fp8q_operand *A, const fp8q_operand *B, void *C, int out
   return gemm_common(A, B, C, out_dtype, M, N, K, amax_out, stream);
 }
 
+namespace {
+
+// C [m, n] = A [m, k] . B [n, k]^T for one role, with both operands' scale
+// layouts checked against their shapes first.
+int gemm_role(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t m,
+              int64_t n, int64_t k, cudaStream_t stream) {
+  if (A == nullptr || B == nullptr || m < 0 || n < 0 || k < 0) return FP8Q_ERR_INVALID_ARG;
+  int rc;
+  if ((rc = check_layout(A, m, k)) != FP8Q_OK || (rc = check_layout(B, n, k)) != FP8Q_OK)
+    return rc;
+  return fp8_gemm(A, B, C, out_dtype, m, n, k, stream);
+}
+
+}  // namespace
+
 int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y, int out_dtype,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
   // y [M, N] = x [M, K] . w [N, K]^T
-  return fp8_gemm(x, w, y, out_dtype, M, N, K, stream);
+  return gemm_role(x, w, y, out_dtype, M, N, K, stream);
 }
 
 int fp8_gemm_dgrad(const fp8q_operand *g, const fp8q_operand *w_t, void *dx, int out_dtype,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
   // dx [M, K] = g [M, N] . (w_t [K, N])^T, contraction over N
-  return fp8_gemm(g, w_t, dx, out_dtype, M, K, N, stream);
+  return gemm_role(g, w_t, dx, out_dtype, M, K, N, stream);
 }
 
 int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw, int out_dtype,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
   // dw [N, K] = g_t [N, M] . (x_t [K, M])^T, contraction over M
-  return fp8_gemm(g_t, x_t, dw, out_dtype, N, K, M, stream);
+  return gemm_role(g_t, x_t, dw, out_dtype, N, K, M, stream);
 }
 
 size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || K < 0) return 0;
+  if (!linear_dims_ok(M, N, K)) return 0;
   size_t b = round256((size_t)(M * K)) + round256((size_t)(N * K));  // FP8 copies of x, w
   b += 2 * round256(sizeof(float)) * 2;                               // amax + scale for x, w
   if (recipe == FP8Q_RECIPE_BLOCK) {
@@ -481,7 +530,7 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M, i
                         fp8q_amax_history *hist_w, void *y, int out_dtype, void *workspace,
                         size_t ws_bytes, cudaStream_t stream) {
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0 || K % 16 != 0 || N % 16 != 0) return FP8Q_ERR_INVALID_ARG;
+  if (!linear_dims_ok(M, N, K) || K % 16 != 0 || N % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   if (recipe != FP8Q_RECIPE_TENSOR_CURRENT && recipe != FP8Q_RECIPE_TENSOR_DELAYED &&
       recipe != FP8Q_RECIPE_BLOCK)
     return FP8Q_ERR_INVALID_ARG;

@@ -18,6 +18,10 @@ unsigned int *device_error_word();
 // SM count of the current device (cached).
 int sm_count();
 
+// True when M, N, K are non-negative and M*K, N*K (and the byte sums of a
+// linear layer's workspace) fit in int64.  Defined in fp8q_api.cu.
+bool linear_dims_ok(int64_t M, int64_t N, int64_t K);
+
 // 2D tiled tensor map over a row-major matrix (outer rows of `inner`
 // elements, rows row_stride_bytes apart); out-of-bounds elements read as
 // zero.  False if the driver entry point is missing or rejects the shape.

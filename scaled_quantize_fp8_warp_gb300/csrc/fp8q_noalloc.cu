@@ -58,7 +58,9 @@ extern "C" int fp8_linear_autocast_noalloc(const void *x, const void *w, int in_
                                            fp8q_amax_history *hist_x,
                                            fp8q_amax_history *hist_w, void *y, int out_dtype,
                                            cudaStream_t stream) {
-  if (M < 0 || N < 0 || K < 0) return FP8Q_ERR_INVALID_ARG;
+  // Negative sizes, or sizes whose byte counts overflow, never reach the
+  // size check below (whose result could otherwise wrap under the limit).
+  if (!fp8q::linear_dims_ok(M, N, K)) return FP8Q_ERR_INVALID_ARG;
   // Reject sizes whose scratch does not fit before touching the device.
   const size_t need = fp8q_linear_workspace_size(recipe, M, N, K);
   if (need > (size_t)FP8Q_NOALLOC_SCRATCH_BYTES) return FP8Q_ERR_WORKSPACE;

@@ -141,6 +141,87 @@ def test_validation_before_device(lib):
                                    aligned, fq.DT_BF16, aligned, 1 << 30, None) == 1
 
 
+def _has_cuda_device():
+    import torch
+    return torch.cuda.is_available()
+
+
+@pytest.mark.skipif(_has_cuda_device(),
+                    reason="valid layouts would reach a kernel launch on placeholder pointers")
+def test_role_wrappers_reject_undocumented_scale_layouts(lib):
+    """fp8_gemm_fprop/_dgrad/_wgrad know each operand's [rows, K] and accept
+    only the scale strides the quantize calls write; anything else would index
+    past the scale array on the device, so it is refused before any device
+    work (INVALID_ARG, 1).  A documented layout passes validation and then
+    fails only at the device check (CUDA, 6: there is no GPU here)."""
+    import scaled_quantize_fp8_warp_gb300 as fq
+    P = ctypes.c_void_p
+    y = P(0x40000)
+    M, N, K = 256, 384, 512
+    ten = fq.Operand(0x10000, fq.E4M3, fq.SCALE_TENSOR, 0x20000, 0, 0)
+
+    def fprop(a, b):
+        return lib.fp8_gemm_fprop(ctypes.byref(a), ctypes.byref(b), y, fq.DT_BF16, M, N, K, None)
+
+    def tile(rows, sr, sk):
+        return fq.Operand(0x10000, fq.E4M3, fq.SCALE_TILE_1x128, 0x20000, sr, sk)
+
+    def block(sr, sk):
+        return fq.Operand(0x10000, fq.E4M3, fq.SCALE_BLOCK_128x128, 0x20000, sr, sk)
+
+    # x [M, K] with 1x128 tiles: stride_row 1, stride_k M
+    assert fprop(tile(M, 1, M), ten) == 6
+    assert fprop(tile(M, 1, M - 16), ten) == 1
+    assert fprop(tile(M, M, 1), ten) == 1
+    # w [N, K] with 128x128 blocks: (ceil(K/128), 1) or, read transposed, (1, ceil(N/128))
+    xt = tile(M, 1, M)
+    assert fprop(xt, block(K // 128, 1)) == 6
+    assert fprop(xt, block(1, 3)) == 6
+    assert fprop(xt, block(1, 4)) == 1
+    assert fprop(xt, block(K // 128 + 1, 1)) == 1
+    # row scales: stride_row 1
+    rowop = fq.Operand(0x10000, fq.E4M3, fq.SCALE_ROW, 0x20000, 1, 0)
+    assert fprop(rowop, rowop) == 6
+    rowbad = fq.Operand(0x10000, fq.E4M3, fq.SCALE_ROW, 0x20000, 2, 0)
+    assert fprop(rowbad, rowop) == 1
+    # dgrad: g [M, N] tiles need stride_k M; w_t [K, N] blocks of w read transposed
+    g = tile(M, 1, M)
+    wt = block(1, K // 128)
+    assert lib.fp8_gemm_dgrad(ctypes.byref(g), ctypes.byref(wt), y, fq.DT_BF16, M, N, K,
+                              None) == 6
+    assert lib.fp8_gemm_dgrad(ctypes.byref(g), ctypes.byref(block(1, N // 128)), y,
+                              fq.DT_BF16, M, N, K, None) == 1
+    # wgrad: g_t [N, M] and x_t [K, M] column tiles: stride_k = N and K respectively
+    gt, xt2 = tile(N, 1, N), tile(K, 1, K)
+    assert lib.fp8_gemm_wgrad(ctypes.byref(gt), ctypes.byref(xt2), y, fq.DT_BF16, M, N, K,
+                              None) == 6
+    assert lib.fp8_gemm_wgrad(ctypes.byref(xt2), ctypes.byref(gt), y, fq.DT_BF16, M, N, K,
+                              None) == 1
+
+
+def test_linear_sizes_that_overflow_are_rejected(lib):
+    """M*K or N*K past int64 must not wrap into a small workspace size: the
+    size query returns 0 and both forwards return INVALID_ARG (1) before any
+    device work -- in particular the workspace-free forward, whose scratch
+    limit check would otherwise pass on a wrapped size."""
+    import scaled_quantize_fp8_warp_gb300 as fq
+    P = ctypes.c_void_p
+    big, K = 1 << 40, 1 << 30
+    for recipe in (fq.RECIPE_TENSOR_CURRENT, fq.RECIPE_BLOCK):
+        assert lib.fp8q_linear_workspace_size(recipe, big, 16, K) == 0
+        assert lib.fp8q_linear_workspace_size(recipe, 16, big, K) == 0
+        assert lib.fp8_linear_autocast(P(0x10000), P(0x10000), fq.DT_BF16, big, 16, K, recipe,
+                                       None, None, P(0x10000), fq.DT_BF16, P(0x10000), 1 << 62,
+                                       None) == 1
+        assert lib.fp8_linear_autocast_noalloc(P(0x10000), P(0x10000), fq.DT_BF16, 16, big, K,
+                                               recipe, None, None, P(0x10000), fq.DT_BF16,
+                                               None) == 1
+    # products that wrap to exactly 2^64 (0 mod 2^64) are caught too
+    assert lib.fp8q_linear_workspace_size(fq.RECIPE_TENSOR_CURRENT, 1 << 34, 16, 1 << 30) == 0
+    # a size that fits is still computed
+    assert lib.fp8q_linear_workspace_size(fq.RECIPE_TENSOR_CURRENT, 1 << 20, 16, 1 << 20) > 0
+
+
 def test_workspace_size_formula(lib):
     import scaled_quantize_fp8_warp_gb300 as fq
     M, N, K = 15872, 4096, 4096

@@ -28,6 +28,8 @@ SCALE_TENSOR = 0
 SCALE_TILE = 1
 SCALE_BLOCK = 2
 SCALE_ROW = 3
+SCALE_MX = 4
+MX_BLOCK = 32
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8_oracle.c")
@@ -55,7 +57,8 @@ def build(force: bool = False) -> str:
 class Operand(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("fmt", ctypes.c_int32),
                 ("scaling", ctypes.c_int32), ("scale", ctypes.c_void_p),
-                ("stride_row", ctypes.c_int64), ("stride_k", ctypes.c_int64)]
+                ("stride_row", ctypes.c_int64), ("stride_k", ctypes.c_int64),
+                ("mx_scale", ctypes.c_void_p)]
 
 
 def _load():
@@ -81,7 +84,11 @@ def _load():
             "orc_quantize_delayed": (F32, [P, I32, I64, I64, I32, I32, P, I32, P, P, P]),
             "orc_quantize_rowwise": (None, [P, I32, I64, I64, I32, I32, P, P, P, P]),
             "orc_dequantize": (None, [P, I64, I32, F32, P]),
-            "orc_operand_scale": (F32, [ctypes.POINTER(Operand), I64, I64]),
+            "orc_operand_scale": (F64, [ctypes.POINTER(Operand), I64, I64]),
+            "orc_e8m0_decode": (F64, [ctypes.c_uint8]),
+            "orc_mx_scale_code": (ctypes.c_uint8, [F32, I32]),
+            "orc_quantize_mx_rows": (None, [P, I32, I64, I64, I32, P, P]),
+            "orc_quantize_mx_cols": (None, [P, I32, I64, I64, I32, P, P]),
             "orc_gemm_points": (None, [ctypes.POINTER(Operand), ctypes.POINTER(Operand),
                                        I64, I64, P, P, P, P]),
             "orc_gemm_rows": (None, [ctypes.POINTER(Operand), ctypes.POINTER(Operand),
@@ -242,6 +249,41 @@ def quantize_delayed(x: np.ndarray, fmt: int, history: np.ndarray, next_slot: in
     return q, qt, np.float32(s), h, nxt.value
 
 
+# ------------------------------------------------------------------ MXFP8
+
+def e8m0_decode(codes) -> np.ndarray:
+    """E8M0 scale bytes -> 2^(code - 127) (NaN for 0xFF)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e8m0_decode(int(b)) for b in c.ravel()],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def mx_scale_code(amax: float, fmt: int) -> int:
+    return int(_load().orc_mx_scale_code(float(amax), fmt))
+
+
+def quantize_mx_rows(x: np.ndarray, fmt: int):
+    """MXFP8 1x32 blocks along each row: (q [R, C], scales [R, ceil(C/32)] E8M0)."""
+    x, dt = _input(x)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    sc = np.empty((rows, (cols + MX_BLOCK - 1) // MX_BLOCK), np.uint8)
+    _load().orc_quantize_mx_rows(_ptr(x), dt, rows, cols, fmt, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def quantize_mx_cols(x: np.ndarray, fmt: int):
+    """MXFP8 32x1 blocks down each column, written transposed:
+    (q_t [C, R], scales [C, ceil(R/32)] E8M0)."""
+    x, dt = _input(x)
+    rows, cols = x.shape
+    qt = np.empty((cols, rows), np.uint8)
+    sc = np.empty((cols, (rows + MX_BLOCK - 1) // MX_BLOCK), np.uint8)
+    _load().orc_quantize_mx_cols(_ptr(x), dt, rows, cols, fmt, _ptr(qt), _ptr(sc))
+    return qt, sc
+
+
 def dequantize(q: np.ndarray, fmt: int, s: float) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     d = np.empty(q.shape, np.float32)
@@ -262,10 +304,16 @@ class GemmOperand:
     def __init__(self, data: np.ndarray, fmt: int, scaling: int = SCALE_TENSOR,
                  scale=None, stride_row: int = 0, stride_k: int = 0):
         self.data = np.ascontiguousarray(data, dtype=np.uint8)
-        self.scale = np.ascontiguousarray(np.atleast_1d(np.asarray(scale, dtype=np.float32)))
         self.rows, self.K = self.data.shape
+        if scaling == SCALE_MX:
+            self.mx = np.ascontiguousarray(np.asarray(scale, dtype=np.uint8))
+            self.scale = np.zeros(1, np.float32)
+            mx_ptr = self.mx.ctypes.data
+        else:
+            self.scale = np.ascontiguousarray(np.atleast_1d(np.asarray(scale, dtype=np.float32)))
+            mx_ptr = None
         self.struct = Operand(self.data.ctypes.data, fmt, scaling, self.scale.ctypes.data,
-                              stride_row, stride_k)
+                              stride_row, stride_k, mx_ptr)
 
     @classmethod
     def tensor(cls, q, fmt, s):
@@ -280,6 +328,13 @@ class GemmOperand:
     def row(cls, q, fmt, scales):
         """One scale per row over all of K (scales [rows])."""
         return cls(q, fmt, SCALE_ROW, scales, stride_row=1, stride_k=0)
+
+    @classmethod
+    def mx(cls, q, fmt, scales):
+        """MXFP8: E8M0 codes [rows, ceil(K/32)] row-major (as quantize_mx_rows
+        and quantize_mx_cols return them)."""
+        sc = np.asarray(scales, dtype=np.uint8)
+        return cls(q, fmt, SCALE_MX, sc, stride_row=sc.shape[1], stride_k=1)
 
     @classmethod
     def block(cls, q, fmt, scales, transposed=False):

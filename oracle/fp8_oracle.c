@@ -95,7 +95,9 @@ static double round_to_grid(double a, fmt_desc d) {
   return r * quantum;       /* exact */
 }
 
-uint8_t orc_fp8_encode(float v, int fmt, int saturate) {
+/* Round-to-nearest-even of a double into the format (see orc_fp8_encode);
+ * every fp32 value is exact in double, so the fp32 entry point is this one. */
+static uint8_t encode_double(double v, int fmt, int saturate) {
   fmt_desc d = describe(fmt);
   uint8_t sign = signbit(v) ? 0x80 : 0x00;
   if (isnan(v)) return (uint8_t)(sign | 0x7F);
@@ -121,6 +123,10 @@ uint8_t orc_fp8_encode(float v, int fmt, int saturate) {
     mant = (int)(mag / ldexp(1.0, e - d.man_bits)) - (1 << d.man_bits);
   }
   return (uint8_t)(sign | (biased << d.man_bits) | mant);
+}
+
+uint8_t orc_fp8_encode(float v, int fmt, int saturate) {
+  return encode_double((double)v, fmt, saturate);
 }
 
 /* ------------------------------------------------------------ amax / scale */
@@ -316,10 +322,90 @@ void orc_dequantize(const uint8_t *q, int64_t n, int fmt, float s, float *d) {
   for (int64_t i = 0; i < n; ++i) d[i] = (float)orc_fp8_decode(q[i], fmt) * s;
 }
 
+/* ------------------------------------------------------------------ MXFP8 */
+
+double orc_e8m0_decode(uint8_t code) {
+  if (code == 0xFF) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
+/* emax_elem: the exponent of the element format's largest normal value
+ * (E4M3: 448 = 1.75 * 2^8; E5M2: 57344 = 1.75 * 2^15). */
+static int mx_emax_elem(int fmt) {
+  int ex;
+  frexp(describe(fmt).fmax, &ex); /* fmax = f * 2^ex, f in [0.5, 1) */
+  return ex - 1;
+}
+
+/* OCP MX v1.0 conversion, shared exponent: floor(log2(amax)) - emax_elem,
+ * clamped to E8M0's [-127, 127]. */
+uint8_t orc_mx_scale_code(float amax, int fmt) {
+  if (isnan(amax) || isinf(amax)) return 0xFF;
+  int e;
+  if (amax == 0.0f) {
+    e = -127; /* floor(log2 0) = -inf, clamped */
+  } else {
+    int ex;
+    frexp((double)amax, &ex); /* amax = f * 2^ex, f in [0.5, 1): floor(log2) = ex-1 */
+    e = (ex - 1) - mx_emax_elem(fmt);
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+  }
+  return (uint8_t)(e + 127);
+}
+
+/* One block of n elements x[i * stride], i < n: its scale code and bytes. */
+static uint8_t mx_block(const void *x, int in_dtype, int64_t first, int64_t stride,
+                        int64_t n, int fmt, uint8_t *out, int64_t out_stride) {
+  float amax = 0.0f;
+  int nonfinite = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    float a = fabsf(orc_load(x, in_dtype, first + i * stride));
+    if (isnan(a) || isinf(a)) nonfinite = 1;
+    else if (a > amax) amax = a;
+  }
+  uint8_t code = nonfinite ? (uint8_t)0xFF : orc_mx_scale_code(amax, fmt);
+  for (int64_t i = 0; i < n; ++i) {
+    if (code == 0xFF) {
+      out[i * out_stride] = 0x7F;
+    } else {
+      /* V / X = V * 2^-(code - 127): exact in double; saturating RNE */
+      double v = ldexp((double)orc_load(x, in_dtype, first + i * stride), 127 - (int)code);
+      out[i * out_stride] = encode_double(v, fmt, 1);
+    }
+  }
+  return code;
+}
+
+void orc_quantize_mx_rows(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, uint8_t *q, uint8_t *scales) {
+  int64_t nb = (cols + ORC_MX_BLOCK - 1) / ORC_MX_BLOCK;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t j = 0; j < nb; ++j) {
+      int64_t c0 = j * ORC_MX_BLOCK;
+      int64_t n = cols - c0 < ORC_MX_BLOCK ? cols - c0 : ORC_MX_BLOCK;
+      scales[r * nb + j] = mx_block(x, in_dtype, r * cols + c0, 1, n, fmt, q + r * cols + c0, 1);
+    }
+}
+
+void orc_quantize_mx_cols(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, uint8_t *q_t, uint8_t *scales) {
+  int64_t nb = (rows + ORC_MX_BLOCK - 1) / ORC_MX_BLOCK;
+  for (int64_t c = 0; c < cols; ++c)
+    for (int64_t j = 0; j < nb; ++j) {
+      int64_t r0 = j * ORC_MX_BLOCK;
+      int64_t n = rows - r0 < ORC_MX_BLOCK ? rows - r0 : ORC_MX_BLOCK;
+      scales[c * nb + j] =
+          mx_block(x, in_dtype, r0 * cols + c, cols, n, fmt, q_t + c * rows + r0, 1);
+    }
+}
+
 /* -------------------------------------------------------------------- GEMM */
 
-float orc_operand_scale(const orc_operand *op, int64_t row, int64_t k) {
+double orc_operand_scale(const orc_operand *op, int64_t row, int64_t k) {
   int64_t kb = k / 128;
+  if (op->scaling == ORC_SCALE_MX)
+    return orc_e8m0_decode(op->mx_scale[row * op->stride_row + (k / ORC_MX_BLOCK) * op->stride_k]);
   if (op->scaling == ORC_SCALE_TENSOR) return op->scale[0];
   if (op->scaling == ORC_SCALE_TILE)
     return op->scale[kb * op->stride_k + row * op->stride_row];
@@ -335,10 +421,8 @@ static void gemm_one(const orc_operand *A, const orc_operand *B, int64_t K,
                      int64_t m, int64_t n, double *y, double *absum) {
   double acc = 0.0, aacc = 0.0;
   for (int64_t k = 0; k < K; ++k) {
-    double a = orc_fp8_decode(A->data[m * K + k], A->fmt) *
-               (double)orc_operand_scale(A, m, k);
-    double b = orc_fp8_decode(B->data[n * K + k], B->fmt) *
-               (double)orc_operand_scale(B, n, k);
+    double a = orc_fp8_decode(A->data[m * K + k], A->fmt) * orc_operand_scale(A, m, k);
+    double b = orc_fp8_decode(B->data[n * K + k], B->fmt) * orc_operand_scale(B, n, k);
     acc += a * b;
     aacc += fabs(a * b);
   }

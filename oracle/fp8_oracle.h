@@ -26,6 +26,10 @@
  *   delayed        -> brute-force ring bookkeeping on short histories
  *   gemm           -> exact rational brute force on tiny shapes, numpy float64
  *                     matmul of decoded operands, closed forms (one-hot rows)
+ *   MX (MXFP8)     -> torch's CPU float8_e8m0fnu decode of every scale byte,
+ *                     the defining bracket of the shared exponent checked in
+ *                     exact rationals, brute-force nearest-value search over
+ *                     all 256 element codes, torch's CPU float8 casts
  * No function here is "parity unpinned".
  */
 #ifndef FP8_ORACLE_H
@@ -52,6 +56,7 @@ extern "C" {
 #define ORC_SCALE_TILE 1   /* one scale per row per 128-wide K block */
 #define ORC_SCALE_BLOCK 2  /* one scale per 128x128 block            */
 #define ORC_SCALE_ROW 3    /* one scale per row over all of K         */
+#define ORC_SCALE_MX 4     /* one E8M0 scale per row per 32-wide K block */
 
 double orc_fmax(int fmt);
 
@@ -127,11 +132,59 @@ float orc_quantize_delayed(const void *x, int in_dtype, int64_t rows,
 /* d[i] = fl32(decode(q[i]) * s). */
 void orc_dequantize(const uint8_t *q, int64_t n, int fmt, float s, float *d);
 
+/* ------------------------------------------------------------------ MXFP8
+ * The Transformer Engine recipe "mxfp8" that the SpikingJelly precision page
+ * lists (fp8_recipe) and that the low-precision-training blog repost uses as
+ * its Blackwell baseline.  The pages give no encoding, so these functions
+ * follow the public OCP Microscaling Formats (MX) Specification v1.0:
+ *   - a block is ORC_MX_BLOCK = 32 consecutive elements along a row (the
+ *     contraction dimension of the GEMM operand); the last block of a row
+ *     may be shorter;
+ *   - the block's shared scale X is an E8M0 byte: unsigned 8-bit exponent,
+ *     bias 127, X = 2^(code - 127); code 0xFF is NaN; there is no zero;
+ *   - elements are FP8 E4M3 or E5M2 (MXFP8);
+ *   - conversion (the specification's vector-to-MX algorithm):
+ *       shared_exp = floor(log2(max_i |V_i|)) - emax_elem, where emax_elem is
+ *       the exponent of the element format's largest normal (8 for E4M3,
+ *       whose largest value is 448 = 1.75 * 2^8; 15 for E5M2, 57344 =
+ *       1.75 * 2^15), clamped to the E8M0 range [-127, 127];
+ *       X = 2^shared_exp;
+ *       P_i = V_i / X rounded to nearest, ties to even, into the element
+ *       format, with finite magnitudes beyond its largest normal clamped to
+ *       it.
+ * Readings where the specification leaves a case open:
+ *   - a block whose elements are all zero has max 0, floor(log2 0) = -inf,
+ *     which the clamp takes to -127: code 0x00, elements +-0;
+ *   - a block holding a NaN or an infinity gets the NaN scale 0xFF; the
+ *     whole block then decodes to NaN whatever its elements hold, and every
+ *     element byte is written as 0x7F (a NaN code in both formats).
+ * V_i / X is exact (X is a power of two and the quotient is formed in
+ * double), so the element rounding is the only rounding. */
+#define ORC_MX_BLOCK 32
+
+/* E8M0 byte -> 2^(code - 127), or NaN for 0xFF. */
+double orc_e8m0_decode(uint8_t code);
+
+/* E8M0 code of the shared scale of a block whose max |V_i| is amax. */
+uint8_t orc_mx_scale_code(float amax, int fmt);
+
+/* 1x32 blocks along each row: q [rows, cols], scales [rows, ceil(cols/32)]
+ * row-major: scale(r, j) = scales[r * ceil(cols/32) + j] for the block of
+ * columns [32 j, min(cols, 32 j + 32)). */
+void orc_quantize_mx_rows(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, uint8_t *q, uint8_t *scales);
+
+/* 32x1 blocks down each column, written transposed: q_t [cols, rows],
+ * scales [cols, ceil(rows/32)].  Exactly orc_quantize_mx_rows of x^T. */
+void orc_quantize_mx_cols(const void *x, int in_dtype, int64_t rows,
+                          int64_t cols, int fmt, uint8_t *q_t, uint8_t *scales);
+
 /* One GEMM operand: data is row-major [rows, K] FP8 bytes.
  *   TENSOR: scale[0]
  *   TILE:   scale[kb * stride_k + row * stride_row]
  *   BLOCK:  scale[(row / 128) * stride_row + kb * stride_k]
  *   ROW:    scale[row * stride_row]
+ *   MX:     e8m0_decode(mx_scale[row * stride_row + (k / 32) * stride_k])
  * with kb = k / 128. */
 typedef struct {
   const uint8_t *data;
@@ -140,10 +193,13 @@ typedef struct {
   const float *scale;
   int64_t stride_row;
   int64_t stride_k;
+  const uint8_t *mx_scale; /* MX only: E8M0 codes */
 } orc_operand;
 
-/* Scale of element (row, k) of an operand, as defined above. */
-float orc_operand_scale(const orc_operand *op, int64_t row, int64_t k);
+/* Scale of element (row, k) of an operand, as defined above (every E8M0
+ * value is exact in double; 2^-127 is an fp32 subnormal, so double is the
+ * return type). */
+double orc_operand_scale(const orc_operand *op, int64_t row, int64_t k);
 
 /* Reference GEMM on a list of output positions:
  *   y[i]     = sum_k decode(A[m,k]) sA(m,k) * decode(B[n,k]) sB(n,k)

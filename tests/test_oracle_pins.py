@@ -520,3 +520,203 @@ def test_gemm_row_scales_vs_numpy():
     ref = (oracle.decode_table(oracle.E4M3)[A] * sa[:, None].astype(np.float64)) @ \
           (oracle.decode_table(oracle.E5M2)[B] * sb[:, None].astype(np.float64)).T
     assert np.all(np.abs(y - ref) <= 1e-13 * ab + 1e-300)
+
+
+# ------------------------------------------------------------------ MXFP8
+# The pages name MXFP8 (the SpikingJelly precision page's fp8_recipe list, the
+# blog repost's Blackwell baseline) but give no encoding; the oracle follows
+# the OCP Microscaling Formats v1.0 specification.  These pins tie it to
+# torch's E8M0 and FP8 casts, to exact rational arithmetic and to a
+# brute-force search, not to its own code.
+
+EMAX_ELEM = {oracle.E4M3: 8, oracle.E5M2: 15}   # 448 = 1.75 * 2^8, 57344 = 1.75 * 2^15
+
+
+def test_e8m0_decode_all_codes_vs_torch():
+    ours = oracle.e8m0_decode(np.arange(256, dtype=np.uint8))
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(
+        torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.isnan(ours[255]) and np.isnan(ref[255])
+    assert np.array_equal(ours[:255], ref[:255])
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_emax_elem_from_the_page_constants(fmt):
+    """emax_elem is the binade of the page's largest value: fmax / 2^emax in [1, 2)."""
+    fm = GOLD["E4M3_MAX" if fmt == oracle.E4M3 else "E5M2_MAX"]["value"]
+    assert 1.0 <= fm / 2.0 ** EMAX_ELEM[fmt] < 2.0
+    # an amax equal to fmax gets scale 1 (code 127): the block needs no scaling
+    assert oracle.mx_scale_code(fm, fmt) == 127
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_mx_scale_bracket_in_exact_rationals(fmt):
+    """X = 2^(code-127) puts the block max in [2^emax, 2^(emax+1)) * X (floor of
+    log2 minus emax_elem), checked with Fractions, except where the E8M0 range
+    clamps the exponent at -127."""
+    rng = np.random.default_rng(30)
+    mags = np.concatenate([
+        2.0 ** rng.uniform(-149, 127.9, 4000),
+        2.0 ** np.arange(-149, 128, dtype=np.float64),             # powers of two
+        np.nextafter(np.float32(2.0) ** np.arange(-120, 127), np.float32(0)),  # just below
+    ]).astype(np.float32)
+    mags = mags[np.isfinite(mags) & (mags > 0)]
+    lo, hi = Fraction(2) ** EMAX_ELEM[fmt], Fraction(2) ** (EMAX_ELEM[fmt] + 1)
+    for a in mags:
+        code = oracle.mx_scale_code(float(a), fmt)
+        assert 0 <= code <= 254
+        X = Fraction(2) ** (code - 127)
+        r = Fraction(float(a)) / X
+        if code == 0:
+            assert r < hi          # clamped at the bottom of E8M0
+        else:
+            assert lo <= r < hi, (a, code)
+
+
+def test_mx_scale_special_cases():
+    for fmt in BOTH:
+        assert oracle.mx_scale_code(0.0, fmt) == 0
+        assert oracle.mx_scale_code(float("nan"), fmt) == 255
+        assert oracle.mx_scale_code(float("inf"), fmt) == 255
+        # amax = 448 * 2^k -> X = 2^k exactly (E4M3), 57344 * 2^k likewise for E5M2
+        fm = oracle.fmax(fmt)
+        for k in (-20, -3, 0, 5, 40):
+            assert oracle.mx_scale_code(fm * 2.0 ** k, fmt) == 127 + k
+
+
+def _nearest_code_brute(v: Fraction, fmt: int) -> int:
+    """The finite FP8 code nearest to v, ties to the even code (mantissa LSB
+    0), magnitudes beyond the largest finite value clamped -- by search over
+    every finite code."""
+    table = oracle.decode_table(fmt)
+    best = None
+    for c in range(256):
+        t = table[c]
+        if not np.isfinite(t):
+            continue
+        d = abs(Fraction(t) - v)
+        key = (d, c & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    c = best[1]
+    # zero keeps the sign of the value (a negative value that rounds to zero is -0)
+    if table[c] == 0:
+        c = 0x80 if v < 0 else 0x00
+    return c
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_mx_elements_are_the_nearest_value_brute_force(fmt):
+    rng = np.random.default_rng(31)
+    # three rows: moderate values with a wide spread, values that hit the
+    # clamp (block max just below the next power of two), and tiny values
+    x = np.empty((3, 64), np.float32)
+    x[0] = rng.standard_normal(64) * 2.0 ** rng.integers(-6, 6, 64)
+    x[1] = rng.uniform(-1, 1, 64)
+    x[1, 5] = 1.999
+    x[1, 40] = -1.99
+    x[2] = rng.standard_normal(64) * 1e-30
+    q, sc = oracle.quantize_mx_rows(x, fmt)
+    for r in range(3):
+        for j in range(2):
+            X = Fraction(2) ** (int(sc[r, j]) - 127)
+            for c in range(32 * j, 32 * j + 32):
+                want = _nearest_code_brute(Fraction(float(x[r, c])) / X, fmt)
+                assert q[r, c] == want, (r, c, x[r, c], q[r, c], want)
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_mx_elements_vs_torch_cast(fmt):
+    """Bytes equal torch's CPU cast of clamp(V / X, +-fmax) (bf16 inputs)."""
+    rng = np.random.default_rng(32)
+    x = (torch.from_numpy(rng.standard_normal((64, 256)).astype(np.float32)) *
+         torch.from_numpy(2.0 ** rng.integers(-10, 10, (64, 1)).astype(np.float32)))
+    xb = x.to(torch.bfloat16)
+    q, sc = oracle.quantize_mx_rows(xb.view(torch.int16).numpy().view(np.uint16), fmt)
+    X = torch.from_numpy(np.ldexp(1.0, sc.astype(np.int64) - 127)).repeat_interleave(32, dim=1)
+    fm = oracle.fmax(fmt)
+    v = (xb.double() / X).clamp(-fm, fm).float()       # exact: X is a power of two
+    ref = v.to(FMT[fmt]).view(torch.uint8).numpy()
+    assert np.array_equal(q, ref)
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_mx_zero_nonfinite_and_ragged_blocks(fmt):
+    x = np.zeros((2, 80), np.float32)
+    x[0, :32] = -0.0                 # all-zero block with negative zeros
+    x[0, 32:64] = np.linspace(-3, 3, 32)
+    x[0, 50] = np.nan                # a NaN poisons its block only
+    # ragged last block (16 elements) of values exact in both formats
+    x[1, 64:80] = [0.125, 0.1875, 0.25, 0.375, 0.5, 0.75, 1, 1.5, 2, 3, 4, 6, 8, 12, 14, 16]
+    q, sc = oracle.quantize_mx_rows(x, fmt)
+    assert sc.shape == (2, 3)
+    assert sc[0, 0] == 0 and np.all(q[0, :32] == 0x80)
+    assert sc[0, 1] == 255 and np.all(q[0, 32:64] == 0x7F)
+    assert sc[1, 0] == 0 and sc[1, 1] == 0
+    assert sc[1, 2] == 127 + 4 - EMAX_ELEM[fmt]         # max 16 = 2^4
+    d = oracle.decode_table(fmt)[q[1, 64:80]] * 2.0 ** (int(sc[1, 2]) - 127)
+    assert np.array_equal(d, x[1, 64:80].astype(np.float64))
+
+
+@pytest.mark.parametrize("fmt", BOTH)
+def test_mx_cols_is_rows_of_transpose(fmt):
+    rng = np.random.default_rng(33)
+    x = (rng.standard_normal((96, 48)) * 3).astype(np.float32)
+    qt, sct = oracle.quantize_mx_cols(x, fmt)
+    q2, sc2 = oracle.quantize_mx_rows(np.ascontiguousarray(x.T), fmt)
+    assert np.array_equal(qt, q2) and np.array_equal(sct, sc2)
+
+
+@pytest.mark.parametrize("fmt,rel", [(oracle.E4M3, 2.0 ** -4), (oracle.E5M2, 2.0 ** -3)])
+def test_mx_roundtrip_error_bound(fmt, rel):
+    """Elements whose |V/X| is a normal at most fmax come back within half an
+    ulp (the smoke step 1 bound); those between fmax and 2^(emax+1) clamp to
+    fmax * X."""
+    rng = np.random.default_rng(34)
+    x = (rng.standard_normal((128, 128)) * 5).astype(np.float32)
+    q, sc = oracle.quantize_mx_rows(x, fmt)
+    X = np.repeat(np.ldexp(1.0, sc.astype(np.int64) - 127), 32, axis=1)
+    d = oracle.decode_table(fmt)[q] * X
+    r = np.abs(x.astype(np.float64)) / X
+    fm = oracle.fmax(fmt)
+    normal = (r >= 2.0 ** (1 - (7 if fmt == oracle.E4M3 else 15))) & (r <= fm)
+    err = np.abs(d - x) / np.abs(x)
+    assert np.all(err[normal] <= rel)
+    over = r > fm
+    assert np.all(np.abs(d[over]) == fm * X[over])
+
+
+def test_gemm_mx_exact_rational_tiny():
+    rng = np.random.default_rng(35)
+    M, N, K = 4, 3, 80          # three 32-blocks, the last one partial
+    for fa, fb in [(oracle.E4M3, oracle.E4M3), (oracle.E5M2, oracle.E4M3)]:
+        A = _rand_codes(rng, (M, K), fa)
+        B = _rand_codes(rng, (N, K), fb)
+        sa = rng.integers(100, 150, (M, 3)).astype(np.uint8)
+        sb = rng.integers(100, 150, (N, 3)).astype(np.uint8)
+        y, ab = oracle.gemm_rows(oracle.GemmOperand.mx(A, fa, sa), oracle.GemmOperand.mx(B, fb, sb))
+        ta, tb = oracle.decode_table(fa), oracle.decode_table(fb)
+        for m in range(M):
+            for n in range(N):
+                terms = [Fraction(ta[A[m, k]]) * Fraction(2) ** (int(sa[m, k // 32]) - 127) *
+                         Fraction(tb[B[n, k]]) * Fraction(2) ** (int(sb[n, k // 32]) - 127)
+                         for k in range(K)]
+                exact = sum(terms)
+                aexact = sum(abs(t) for t in terms)
+                assert abs(Fraction(y[m, n]) - exact) <= Fraction(1, 2 ** 50) * aexact
+                assert abs(Fraction(ab[m, n]) - aexact) <= Fraction(1, 2 ** 50) * aexact
+
+
+def test_gemm_mx_vs_numpy_dense():
+    rng = np.random.default_rng(36)
+    M, N, K = 70, 90, 256
+    fa, fb = oracle.E5M2, oracle.E4M3
+    A = _rand_codes(rng, (M, K), fa)
+    B = _rand_codes(rng, (N, K), fb)
+    sa = rng.integers(110, 140, (M, K // 32)).astype(np.uint8)
+    sb = rng.integers(110, 140, (N, K // 32)).astype(np.uint8)
+    Ad = oracle.decode_table(fa)[A] * np.repeat(np.ldexp(1.0, sa.astype(np.int64) - 127), 32, 1)
+    Bd = oracle.decode_table(fb)[B] * np.repeat(np.ldexp(1.0, sb.astype(np.int64) - 127), 32, 1)
+    y, ab = oracle.gemm_rows(oracle.GemmOperand.mx(A, fa, sa), oracle.GemmOperand.mx(B, fb, sb))
+    assert np.all(np.abs(y - Ad @ Bd.T) <= 1e-13 * ab + 1e-300)
+    assert np.allclose(ab, np.abs(Ad) @ np.abs(Bd).T, rtol=1e-13)

@@ -83,13 +83,15 @@ typedef enum fp8q_scaling {
   FP8Q_SCALE_TENSOR = 0,      /* one scale for the whole operand */
   FP8Q_SCALE_TILE_1x128 = 1,  /* one scale per row per 128-wide K block */
   FP8Q_SCALE_BLOCK_128x128 = 2, /* one scale per 128x128 block */
-  FP8Q_SCALE_ROW = 3            /* one scale per row over all of K */
+  FP8Q_SCALE_ROW = 3,           /* one scale per row over all of K */
+  FP8Q_SCALE_MX_1x32 = 4        /* MXFP8: one E8M0 scale per row per 32 K */
 } fp8q_scaling;
 
 typedef enum fp8q_recipe {
   FP8Q_RECIPE_TENSOR_CURRENT = 0, /* per-tensor, scale from this tensor's amax */
   FP8Q_RECIPE_TENSOR_DELAYED = 1, /* per-tensor, scale from an amax history */
-  FP8Q_RECIPE_BLOCK = 2           /* 1x128 tiles on x, 128x128 blocks on w */
+  FP8Q_RECIPE_BLOCK = 2,          /* 1x128 tiles on x, 128x128 blocks on w */
+  FP8Q_RECIPE_MXFP8 = 3           /* MXFP8 1x32 blocks on x and w */
 } fp8q_recipe;
 
 /* Length of the delayed-scaling amax history ([fp8_parity] smoke step 3 keeps
@@ -234,6 +236,43 @@ int fp8_quantize_rowwise(const void *x, int in_dtype, int64_t rows,
                          uint8_t *q_t, float *qt_scales, int saturate,
                          cudaStream_t stream);
 
+/* MXFP8 ([sj_precision] lists "mxfp8" among Transformer Engine's fp8_recipe
+ * choices; [te_blog] "Decoding the results for a real model" uses MXFP8 as its
+ * Blackwell baseline).  The pages give no encoding; this follows the OCP
+ * Microscaling Formats (MX) Specification v1.0:
+ *   - blocks of 32 consecutive elements share one E8M0 scale byte
+ *     X = 2^(code - 127) (0xFF = NaN);
+ *   - code = floor(log2(max |x|)) - emax + 127, clamped to [0, 254], with
+ *     emax = 8 (E4M3, 448 = 1.75 * 2^8) or 15 (E5M2, 57344 = 1.75 * 2^15);
+ *     an all-zero block gets code 0;
+ *   - byte = RNE(x / X) into `format`, saturating at +-fmax (exact: X is a
+ *     power of two);
+ *   - a block holding a NaN or an infinity gets code 0xFF and every byte
+ *     0x7F (it decodes to NaN whatever its bytes).
+ * One read of x produces either or both of
+ *   q [rows, cols] with 1x32 blocks along each row (q_scales), and
+ *   q_t [cols, rows] (the transpose) with 32x1 blocks down each column of x,
+ *     i.e. 1x32 blocks along each row of q_t (qt_scales) -- the operand
+ *     Dgrad's and Wgrad's contractions need.
+ * Scale layout ("atoms", what the MXFP8 GEMM copies to the tensor cores as
+ * is): for an operand [R, K] (q: R = rows, K = cols; q_t: R = cols,
+ * K = rows), one 512-byte atom per 128-row x 128-K tile; the atom of row
+ * block rb and K block kb starts at byte (rb * ceil(K/128) + kb) * 512, and
+ * the scale of row 128 rb + r, 32-wide K block 4 kb + j (r < 128, j < 4) is
+ * byte (r % 32) * 16 + (r / 32) * 4 + j of it.  Rows and K blocks past the
+ * matrix hold code 0.  Each array takes fp8q_mx_scale_bytes(rows, cols).
+ * cols % 16 == 0; rows % 16 == 0 when the q_t pair is requested.  Each pair
+ * is both-or-neither; at least one.  Scale arrays 16-byte aligned.
+ * Errors: INVALID_ARG, MISALIGNED, ARCH, CUDA. */
+int fp8_quantize_mxfp8(const void *x, int in_dtype, int64_t rows, int64_t cols,
+                       int format, uint8_t *q, uint8_t *q_scales, uint8_t *q_t,
+                       uint8_t *qt_scales, cudaStream_t stream);
+
+/* Bytes of one orientation's MXFP8 scale atoms for an [rows, cols] matrix:
+ * ceil(rows/128) * ceil(cols/128) * 512 (the same for the transpose); 0 for
+ * negative sizes. */
+size_t fp8q_mx_scale_bytes(int64_t rows, int64_t cols);
+
 /* 128x128 block scaling for weights ([te_blog] "2D block scaling for
  * weights"): one scale per block, block_scales [ceil(rows/128),
  * ceil(cols/128)] row-major; q [rows, cols] and/or q_t [cols, rows] (the same
@@ -254,6 +293,9 @@ int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows,
  *   FP8Q_SCALE_TILE_1x128:    scale[kb * scale_stride_k + row * scale_stride_row]
  *   FP8Q_SCALE_BLOCK_128x128: scale[(row/128) * scale_stride_row + kb * scale_stride_k]
  *   FP8Q_SCALE_ROW:           scale[row * scale_stride_row]
+ *   FP8Q_SCALE_MX_1x32:       2^(mx_scale byte of (row, k / 32) - 127), the
+ *                             byte found through the atom layout of
+ *                             fp8_quantize_mxfp8 (strides unused, 0)
  * (scale in device memory).  The quantize calls above produce:
  *   tile scales of an [R, K] matrix:   stride_row = 1, stride_k = R
  *   block scales of an [R, K] matrix:  stride_row = ceil(K/128), stride_k = 1
@@ -268,7 +310,12 @@ typedef struct fp8q_operand {
   const uint8_t *data;
   int32_t format;
   int32_t scaling;
-  const float *scale;
+  union {
+    const float *scale;       /* TENSOR, TILE_1x128, BLOCK_128x128, ROW */
+    const uint8_t *mx_scale;  /* MX_1x32: E8M0 atoms (fp8_quantize_mxfp8
+                                 layout for this [rows, K] operand), 16-byte
+                                 aligned; both strides must be 0 */
+  };
   int64_t scale_stride_row;
   int64_t scale_stride_k;
 } fp8q_operand;
@@ -282,7 +329,9 @@ typedef struct fp8q_operand {
  *   A: [M, K], B: [N, K]; N % 16 == 0, K % 16 == 0; M >= 0 any.
  *   M == 0 or N == 0: nothing to do.  K == 0: C is zero.
  * Supported combinations: TENSOR/ROW with TENSOR/ROW (scales applied in the
- * epilogue), and A TILE with B TILE or BLOCK (promoted per K block).
+ * epilogue), A TILE with B TILE or BLOCK (promoted per K block), and MX_1x32
+ * with MX_1x32 (the tensor cores apply the E8M0 scales per 32 K; MX atoms of
+ * K blocks past K must hold finite codes, as fp8_quantize_mxfp8 writes).
  * Errors: INVALID_ARG, MISALIGNED, ARCH, NOT_IMPLEMENTED (other combinations),
  * CUDA. */
 int fp8_gemm(const fp8q_operand *A, const fp8q_operand *B, void *C,
@@ -344,6 +393,7 @@ size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K);
  *   TENSOR_CURRENT: amax(x), amax(w), cast x, cast w, per-tensor GEMM
  *   TENSOR_DELAYED: casts with hist_x / hist_w (device state, required)
  *   BLOCK:          1x128 row tiles of x, 128x128 blocks of w, promoted GEMM
+ *   MXFP8:          1x32 MXFP8 blocks of x and w, block-scaled MMA
  *   workspace  device scratch of at least fp8q_linear_workspace_size bytes,
  *              256-byte aligned; holds the FP8 copies, scales and amaxes
  * Alignment: K % 16 == 0, N % 16 == 0.

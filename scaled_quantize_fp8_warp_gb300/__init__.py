@@ -28,9 +28,12 @@ SCALE_TENSOR = 0
 SCALE_TILE_1x128 = 1
 SCALE_BLOCK_128x128 = 2
 SCALE_ROW = 3
+SCALE_MX_1x32 = 4
 RECIPE_TENSOR_CURRENT = 0
 RECIPE_TENSOR_DELAYED = 1
 RECIPE_BLOCK = 2
+RECIPE_MXFP8 = 3
+MX_BLOCK = 32
 HISTORY_LEN = 16
 HISTORY_BYTES = 80
 
@@ -47,7 +50,8 @@ EXPORTS = (
     "fp8q_selftest_barrier_timeout", "fp8_amax",
     "fp8_quantize_tensor", "fp8_quantize_tensor_current", "fp8_quantize_delayed",
     "fp8q_history_init",
-    "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_block128x128", "fp8_gemm",
+    "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_mxfp8",
+    "fp8q_mx_scale_bytes", "fp8_quantize_block128x128", "fp8_gemm",
     "fp8_gemm_amax", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
     "fp8_linear_autocast_noalloc",
@@ -97,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8_quantize_tile1x128": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
             "fp8_quantize_block128x128": (I32, [P, I32, I64, I64, I32, P, P, P, I32, P]),
+            "fp8_quantize_mxfp8": (I32, [P, I32, I64, I64, I32, P, P, P, P, P]),
+            "fp8q_mx_scale_bytes": (SZ, [I64, I64]),
             "fp8_gemm": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_amax": (I32, [OP, OP, P, I32, I64, I64, I64, P, P]),
             "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
@@ -297,6 +303,32 @@ def fp8_quantize_rowwise(x, fmt, rows=True, cols=False, saturate=False, q=None, 
     return ((q, q_scales) if rows else (None, None)) + ((q_t, qt_scales) if cols else (None, None))
 
 
+def mx_scale_bytes(rows: int, cols: int) -> int:
+    """Bytes of one orientation's MXFP8 scale atoms for an [rows, cols] matrix."""
+    return int(lib().fp8q_mx_scale_bytes(rows, cols))
+
+
+def fp8_quantize_mxfp8(x, fmt, rows=True, cols=False, q=None, q_scales=None, q_t=None,
+                       qt_scales=None, stream=None):
+    """MXFP8 (OCP MX v1.0): q [R,C] with 1x32 row blocks and/or q_t [C,R] with
+    32x1 column blocks of x; scales are E8M0 bytes in the library's atom
+    layout (uint8 tensors of mx_scale_bytes(R, C) bytes; see include/fp8q.h).
+    Returns (q, q_scales, q_t, qt_scales), None for a pair not requested."""
+    R, C = _rows_cols(x)
+    nbytes = mx_scale_bytes(R, C)
+    if rows:
+        q = q if q is not None else _empty((R, C), torch.uint8, x)
+        q_scales = q_scales if q_scales is not None else _empty((nbytes,), torch.uint8, x)
+    if cols:
+        q_t = q_t if q_t is not None else _empty((C, R), torch.uint8, x)
+        qt_scales = qt_scales if qt_scales is not None else _empty((nbytes,), torch.uint8, x)
+    _check(lib().fp8_quantize_mxfp8(
+        _ptr(x), _in_dtype(x), R, C, fmt, _ptr(q if rows else None),
+        _ptr(q_scales if rows else None), _ptr(q_t if cols else None),
+        _ptr(qt_scales if cols else None), _stream(stream)), "fp8_quantize_mxfp8")
+    return ((q, q_scales) if rows else (None, None)) + ((q_t, qt_scales) if cols else (None, None))
+
+
 def fp8_quantize_block128x128(x, fmt, want_q=True, want_qt=False, saturate=False, q=None,
                               q_t=None, scales=None, stream=None):
     R, C = _rows_cols(x)
@@ -342,6 +374,11 @@ class GemmOperand:
     def row(cls, q, fmt, scales):
         """One scale per row over all of K (scales [rows])."""
         return cls(q, fmt, SCALE_ROW, scales, 1, 0)
+
+    @classmethod
+    def mx(cls, q, fmt, atoms):
+        """MXFP8 operand: atoms as fp8_quantize_mxfp8 writes them for q."""
+        return cls(q, fmt, SCALE_MX_1x32, atoms, 0, 0)
 
     @classmethod
     def block(cls, q, fmt, scales):

@@ -88,9 +88,15 @@ int check_ptr(const void *p, bool required) {
 int check_operand(const fp8q_operand *op, int64_t rows, int64_t K) {
   if (op == nullptr || !valid_format(op->format)) return FP8Q_ERR_INVALID_ARG;
   if (op->scaling != FP8Q_SCALE_TENSOR && op->scaling != FP8Q_SCALE_TILE_1x128 &&
-      op->scaling != FP8Q_SCALE_BLOCK_128x128 && op->scaling != FP8Q_SCALE_ROW)
+      op->scaling != FP8Q_SCALE_BLOCK_128x128 && op->scaling != FP8Q_SCALE_ROW &&
+      op->scaling != FP8Q_SCALE_MX_1x32)
     return FP8Q_ERR_INVALID_ARG;
   if (op->scale == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (op->scaling == FP8Q_SCALE_MX_1x32) {
+    // atoms are fetched with 16-byte bulk copies; the layout has no strides
+    if (!aligned16(op->mx_scale)) return FP8Q_ERR_MISALIGNED;
+    if (op->scale_stride_row != 0 || op->scale_stride_k != 0) return FP8Q_ERR_INVALID_ARG;
+  }
   if ((reinterpret_cast<uintptr_t>(op->scale) & 3u) != 0) return FP8Q_ERR_MISALIGNED;
   if (op->scaling != FP8Q_SCALE_TENSOR && (op->scale_stride_row < 0 || op->scale_stride_k < 0))
     return FP8Q_ERR_INVALID_ARG;
@@ -123,6 +129,9 @@ int check_layout(const fp8q_operand *op, int64_t rows, int64_t K) {
                  : FP8Q_ERR_INVALID_ARG;
     case FP8Q_SCALE_ROW:
       return op->scale_stride_row == 1 ? FP8Q_OK : FP8Q_ERR_INVALID_ARG;
+    case FP8Q_SCALE_MX_1x32:
+      return (op->scale_stride_row == 0 && op->scale_stride_k == 0) ? FP8Q_OK
+                                                                     : FP8Q_ERR_INVALID_ARG;
   }
   return FP8Q_ERR_INVALID_ARG;
 }
@@ -133,6 +142,7 @@ GemmOperandDev to_dev(const fp8q_operand *op) {
   d.format = op->format;
   d.scaling = op->scaling;
   d.scale = op->scale;
+  d.mx_scale = op->scaling == FP8Q_SCALE_MX_1x32 ? op->mx_scale : nullptr;
   d.stride_row = op->scale_stride_row;
   d.stride_k = op->scale_stride_k;
   return d;
@@ -417,6 +427,47 @@ int fp8_quantize_rowwise(const void *x, int in_dtype, int64_t rows, int64_t cols
   return FP8Q_OK;
 }
 
+size_t fp8q_mx_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows < 0 || cols < 0) return 0;
+  return (size_t)((rows + 127) / 128) * (size_t)((cols + 127) / 128) * 512u;
+}
+
+int fp8_quantize_mxfp8(const void *x, int in_dtype, int64_t rows, int64_t cols, int format,
+                       uint8_t *q, uint8_t *q_scales, uint8_t *q_t, uint8_t *qt_scales,
+                       cudaStream_t stream) {
+  const bool want_row = q != nullptr || q_scales != nullptr;
+  const bool want_col = q_t != nullptr || qt_scales != nullptr;
+  int rc = check_quant(x, in_dtype, rows, cols, format, want_col);
+  if (rc != FP8Q_OK) return rc;
+  if (rows > 0 && cols > 0) {
+    if (!want_row && !want_col) return FP8Q_ERR_INVALID_ARG;
+    if (want_row && (q == nullptr || q_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+    if (want_col && (q_t == nullptr || qt_scales == nullptr)) return FP8Q_ERR_INVALID_ARG;
+  }
+  if ((rc = check_ptr(q, false)) != FP8Q_OK || (rc = check_ptr(q_t, false)) != FP8Q_OK ||
+      (rc = check_ptr(q_scales, false)) != FP8Q_OK || (rc = check_ptr(qt_scales, false)) != FP8Q_OK)
+    return rc;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  if (rows == 0 || cols == 0) return FP8Q_OK;
+  QuantParams p{};
+  p.x = x;
+  p.rows = rows;
+  p.cols = cols;
+  p.in_dtype = in_dtype;
+  p.format = format;
+  p.saturate = 1;
+  p.mode = kModeMx;
+  p.err = device_error_word();
+  p.q = want_row ? q : nullptr;
+  p.mx_scales = want_row ? q_scales : nullptr;
+  p.q_t = want_col ? q_t : nullptr;
+  p.mxt_scales = want_col ? qt_scales : nullptr;
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] quantize_mxfp8 %lldx%lld fmt=%d rows=%d cols=%d\n", (long long)rows,
+            (long long)cols, format, want_row, want_col);
+  return from_cuda(launch_quant2d(p, stream));
+}
+
 int fp8_quantize_block128x128(const void *x, int in_dtype, int64_t rows, int64_t cols,
                               int format, uint8_t *q, uint8_t *q_t, float *block_scales,
                               int saturate, cudaStream_t stream) {
@@ -521,6 +572,8 @@ size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K) {
   if (recipe == FP8Q_RECIPE_BLOCK) {
     b += round256(sizeof(float) * (size_t)(((K + 127) / 128) * M));    // x tile scales
     b += round256(sizeof(float) * (size_t)(((N + 127) / 128) * ((K + 127) / 128)));
+  } else if (recipe == FP8Q_RECIPE_MXFP8) {
+    b += round256(fp8q_mx_scale_bytes(M, K)) + round256(fp8q_mx_scale_bytes(N, K));
   }
   return b;
 }
@@ -532,7 +585,7 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M, i
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
   if (!linear_dims_ok(M, N, K) || K % 16 != 0 || N % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   if (recipe != FP8Q_RECIPE_TENSOR_CURRENT && recipe != FP8Q_RECIPE_TENSOR_DELAYED &&
-      recipe != FP8Q_RECIPE_BLOCK)
+      recipe != FP8Q_RECIPE_BLOCK && recipe != FP8Q_RECIPE_MXFP8)
     return FP8Q_ERR_INVALID_ARG;
   if (recipe == FP8Q_RECIPE_TENSOR_DELAYED && (hist_x == nullptr || hist_w == nullptr))
     return FP8Q_ERR_INVALID_ARG;
@@ -579,6 +632,20 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M, i
     B.scale = w_scales;
     B.scale_stride_row = (K + 127) / 128;
     B.scale_stride_k = 1;
+  } else if (recipe == FP8Q_RECIPE_MXFP8) {
+    uint8_t *x_atoms = ws;
+    ws += round256(fp8q_mx_scale_bytes(M, K));
+    uint8_t *w_atoms = ws;
+    if ((rc = fp8_quantize_mxfp8(x, in_dtype, M, K, FP8Q_E4M3, qx, x_atoms, nullptr, nullptr,
+                                 stream)) != FP8Q_OK)
+      return rc;
+    if ((rc = fp8_quantize_mxfp8(w, in_dtype, N, K, FP8Q_E4M3, qw, w_atoms, nullptr, nullptr,
+                                 stream)) != FP8Q_OK)
+      return rc;
+    A.scaling = FP8Q_SCALE_MX_1x32;
+    A.mx_scale = x_atoms;
+    B.scaling = FP8Q_SCALE_MX_1x32;
+    B.mx_scale = w_atoms;
   } else {
     if (recipe == FP8Q_RECIPE_TENSOR_CURRENT) {
       if ((rc = fp8_amax(x, in_dtype, M * K, amax_x, stream)) != FP8Q_OK) return rc;

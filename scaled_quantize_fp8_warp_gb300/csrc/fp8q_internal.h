@@ -36,7 +36,8 @@ enum QuantMode : int {
   kModeBlock = 3,          // 128x128 blocks
   kModeRowAmax = 4,        // row-wise pass 1: per-row / per-column amax into the scale arrays
   kModeRowCast = 5,        // row-wise pass 2: cast with per-row / per-column scales
-  kModeTensorFused = 6     // amax and per-tensor cast in one cooperative launch
+  kModeTensorFused = 6,    // amax and per-tensor cast in one cooperative launch
+  kModeMx = 7              // MXFP8: 1x32 row blocks and/or 32x1 column blocks, E8M0 scales
 };
 
 struct QuantParams {
@@ -54,6 +55,8 @@ struct QuantParams {
   uint8_t *q_t;                // [cols, rows] or null
   float *q_scales;             // tile: [ceil(cols/128), rows]; block: [nrb, ncb]
   float *qt_scales;            // tile: [ceil(rows/128), cols]
+  uint8_t *mx_scales;          // MX: E8M0 atoms of q (see fp8_quantize_mxfp8)
+  uint8_t *mxt_scales;         // MX: E8M0 atoms of q_t
   unsigned int *err;           // device error word (bounded waits)
   int work_slot;               // tile-scheduling slot (set at launch)
   int dynamic;                 // 1: tiles past the first few are claimed (set at launch)
@@ -75,6 +78,7 @@ struct GemmOperandDev {
   int format;
   int scaling;
   const float *scale;
+  const uint8_t *mx_scale;   // FP8Q_SCALE_MX_1x32: E8M0 atoms
   int64_t stride_row;
   int64_t stride_k;
 };

@@ -71,6 +71,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // Load into this CTA's shared memory, completion counted on an mbarrier that
 // may sit in the peer CTA of the pair (`bar_cluster` is a shared::cluster
 // address, e.g. from mapa).
@@ -209,6 +219,31 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
       : "memory");
 }
 
+// Block-scaled MMA (kind::mxf8f6f4, one E8M0 scale per 32 K): D[tmem] (+)=
+// (A . SFA) . (B . SFB)^T with the scale factors read from tensor memory at
+// sfa_tmem / sfb_tmem; the instruction descriptor selects the byte of each
+// 32-bit scale word (see idesc_mxf8f6f4).
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t sfa_tmem,
+                                             uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (descriptor `sdesc`) into tensor
+// memory at `taddr`, replicated into each of the four 32-lane quarters: row r
+// lands in lane r of every quarter, its bytes in columns taddr .. taddr + 3.
+// Ordered with this thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread t of the warp receives
 // lane (base lane + t), columns [col, col + 32).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -277,6 +312,29 @@ __device__ __forceinline__ uint64_t sdesc_k(uint32_t saddr, uint32_t sbo, uint32
 __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t afmt, uint32_t bfmt, uint32_t m,
                                                    uint32_t n) {
   return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Shared-memory descriptor of an unswizzled K-major matrix of 16-byte rows:
+// 8-row core matrices of 128 contiguous bytes, `sbo` bytes from one 8-row
+// group to the next (layout type 0 = no swizzle).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling, both operands
+// K-major: byte of B's scale word in [4,6), A / B formats in [7,10) /
+// [10,13) (0 = E4M3, 1 = E5M2), N >> 3 in [17,23), scale type in bit 23
+// (1 = UE8M0), M >> 4 in [24,29), byte of A's scale word in [29,31).
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t afmt, uint32_t bfmt, uint32_t m,
+                                                     uint32_t n, uint32_t sfa_byte,
+                                                     uint32_t sfb_byte) {
+  return (sfb_byte << 4) | (afmt << 7) | (bfmt << 10) | ((n >> 3) << 17) | (1u << 23) |
+         ((m >> 4) << 24) | (sfa_byte << 29);
 }
 
 // Wall-clock limit of every barrier wait in the library's kernels.

@@ -23,6 +23,13 @@
 // is a shuffle butterfly inside each half-warp; column amax for 128x1 tiles
 // goes through shared memory; the transposed FP8 copy is an in-register 8x8
 // byte transpose (uniform scales) or a second cast (column-tile scales).
+//
+// MXFP8 (the "mxfp8" recipe; the pages give no encoding, so the OCP
+// Microscaling Formats v1.0 specification defines it): blocks of 32 elements
+// share an E8M0 scale X = 2^(floor(log2 amax) - emax_elem); the biased
+// exponent of amax's fp32 bit pattern gives that directly, X is a power of
+// two, and the element is the saturating conversion of the exact product
+// x * (1 / X): no division is involved.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -269,6 +276,81 @@ __device__ __forceinline__ uint2 cast_row(const Row8<InT> &x, float s, float r, 
                          x.at(7), s, saturate);
 }
 
+// ------------------------------------------------------------------ MXFP8
+
+// E8M0 code of a block from the fp32 bit pattern of its max |x|.  For a
+// normal max, floor(log2 amax) = E - 127 with E the biased exponent, so the
+// shared exponent floor(log2 amax) - emax_elem is E - 127 - emax_elem and its
+// E8M0 code (bias 127) is E - emax_elem; a zero or subnormal max (E = 0), or
+// any code below E8M0's range, clamps to 0 (2^-127); an Inf or NaN max gives
+// the NaN code 0xFF.  emax_elem: 448 = 1.75 * 2^8, 57344 = 1.75 * 2^15.
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_code(uint32_t amax_bits) {
+  constexpr int kEmax = FMT == FP8Q_E4M3 ? 8 : 15;
+  const int e = (int)(amax_bits >> 23);
+  if (e == 255) return 0xFFu;
+  return (uint32_t)max(e - kEmax, 0);
+}
+
+// 1 / X = 2^(127 - code) for a finite code (0..254): 2^-127 is subnormal.
+__device__ __forceinline__ float mx_inv_scale(uint32_t code) {
+  return code >= 254u ? __uint_as_float(0x00400000u) : __uint_as_float((254u - code) << 23);
+}
+
+// Eight elements times 1/X (exact), saturating RNE to FP8; the sign bits are
+// OR-ed in from the inputs so that a negative value that rounds to zero is
+// -0 (0x80).  A NaN block (code 0xFF) writes 0x7F everywhere.
+template <int FMT>
+__device__ __forceinline__ uint2 mx_cast_row(const Row8<uint16_t> &x, uint32_t code) {
+  if (code == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const float f = mx_inv_scale(code);
+  const float2 f2 = make_float2(f, f);
+  uint32_t p[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t w = x.word(k);
+    p[k] = cvt_pair<FMT>(
+        __fmul2_rn(make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), f2));
+  }
+  const uint32_t lo = __byte_perm(p[0], p[1], 0x5410) |
+                      (__byte_perm(x.w.x, x.w.y, 0x7531) & 0x80808080u);
+  const uint32_t hi = __byte_perm(p[2], p[3], 0x5410) |
+                      (__byte_perm(x.w.z, x.w.w, 0x7531) & 0x80808080u);
+  return make_uint2(lo, hi);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 mx_cast8(const float (&v)[8], uint32_t code) {
+  if (code == 0xFFu) return make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const float f = mx_inv_scale(code);
+  const float2 f2 = make_float2(f, f);
+  uint32_t p[4], sg[2] = {0u, 0u};
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    p[k] = cvt_pair<FMT>(__fmul2_rn(make_float2(v[2 * k], v[2 * k + 1]), f2));
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    sg[j >> 2] |= ((__float_as_uint(v[j]) >> 31) << 7) << (8 * (j & 3));
+  return make_uint2(__byte_perm(p[0], p[1], 0x5410) | sg[0],
+                    __byte_perm(p[2], p[3], 0x5410) | sg[1]);
+}
+
+template <int FMT>
+__device__ __forceinline__ uint2 mx_cast_row(const Row8<float> &x, uint32_t code) {
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = x.at(j);
+  return mx_cast8<FMT>(v, code);
+}
+
+// Byte offset, inside a tile's 512-byte scale atom, of the scale of row r
+// (0..127 of the tile) and 32-wide K block j (0..3): the layout the GEMM's
+// tensor memory copy (32 rows of 16 bytes, replicated over the four lane
+// quarters) turns into what the block-scaled MMA reads.
+__device__ __forceinline__ int mx_atom_offset(int r, int j) {
+  return (r & 31) * 16 + (r >> 5) * 4 + j;
+}
+
 // 4x4 byte transpose: a..d are rows (byte k = column k); o0..o3 are columns.
 __device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d,
                                              uint32_t &o0, uint32_t &o1, uint32_t &o2,
@@ -306,8 +388,10 @@ enum KernelMode : int {
   kKRowAmax = 6,    // row-wise pass 1: per-row / per-column amax, atomicMax into
                     // q_scales / qt_scales (as fp32 bit patterns)
   kKRowCast = 7,    // row-wise pass 2: cast with the scales of those amaxes
-  kKTensorFused = 8 // per-tensor current scaling in one cooperative launch:
-                    // amax over every tile, a grid barrier, then the cast
+  kKTensorFused = 8, // per-tensor current scaling in one cooperative launch:
+                     // amax over every tile, a grid barrier, then the cast
+  kKMx = 9           // MXFP8: 1x32 row blocks -> q and/or 32x1 column blocks
+                     // -> q_t, each with its tile's 512-byte E8M0 atom
 };
 
 // Dynamic tile scheduling: each launch of the quantize kernel takes one slot
@@ -346,11 +430,13 @@ struct QuantShape {
   static constexpr int kStageBytes = kStaging ? 64 * 128 : 0;
   // the column-tile modes' own scratch would not leave room for three
   static constexpr bool kThree = FP8Q_QUANT_MINB3 != 0 && sizeof(InT) == 2 &&
-                                 !(KM == 3 || KM == 4 || KM == 7);
+                                 !(KM == 3 || KM == 4 || KM == 7 || KM == 9);
   static constexpr int kMinBlocks = kThree ? 3 : 2;
   static constexpr int kStages = kThree ? 2 : QuantRing<InT>::kStages;
   static constexpr int kTileBytes = QuantRing<InT>::kTileBytes;
-  static constexpr int kSmemBytes = kStages * kTileBytes + kStageBytes + 1024;
+  // MXFP8: the tile's two 512-byte scale atoms are assembled in shared memory
+  static constexpr int kMxBytes = KM == 9 ? 1024 : 0;
+  static constexpr int kSmemBytes = kStages * kTileBytes + kStageBytes + kMxBytes + 1024;
 };
 
 template <typename InT, int FMT, int KM>
@@ -361,6 +447,7 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
   constexpr bool kRowwise = (KM == kKRowAmax || KM == kKRowCast);
   constexpr bool kFused = (KM == kKTensorFused);
   constexpr bool kUniform = (KM == kKTensor || KM == kKDelayed || KM == kKBlock || kFused);
+  constexpr bool kMx = (KM == kKMx);
   using Ring = QuantShape<InT, KM>;
   const float fm = FmtTraits<FMT>::kMax;
 
@@ -385,6 +472,7 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
   const uint32_t ring = (raw + 1023u) & ~1023u;
   const uint8_t *ring_ptr = dyn_smem + (ring - raw);
   uint8_t *qt_stage = dyn_smem + (ring - raw) + Ring::kStages * Ring::kTileBytes;
+  uint8_t *mx_stage = qt_stage + Ring::kStageBytes;   // MX: rows atom, then columns atom
   volatile int *abort_flag = &sh_abort;
 
   // The transposed FP8 tile (q_t rows c0.., byte columns r0..) goes out as
@@ -564,11 +652,11 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
     uint32_t rowmax[8];
     uint32_t cmp[Row8<InT>::kColWords];
     uint32_t tmax = 0;
-    if (kRowTiles || kUniform || kRowwise) {
+    if (kRowTiles || kUniform || kRowwise || kMx) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) rowmax[i] = v[i].absmax_bits();
     }
-    if (kColTiles || kRowwise) {
+    if (kColTiles || kRowwise || kMx) {
 #pragma unroll
       for (int k = 0; k < Row8<InT>::kColWords; ++k) cmp[k] = 0;
 #pragma unroll
@@ -784,6 +872,79 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
         store_qt(cb, valid, r0, c0);
       }
     }
+    // -------------------------------------------------------------- MXFP8
+    if (kMx) {
+      if (p.q != nullptr) {
+        // 1x32 row blocks: the four lanes cg = 4 b .. 4 b + 3 of a half-warp
+        // hold one block of each of their 8 rows
+        const int jblk = cg >> 2;
+        uint32_t code[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t m = max(rowmax[i], __shfl_xor_sync(0xFFFFFFFFu, rowmax[i], 1));
+          m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+          code[i] = mx_code<FMT>(m);
+        }
+        if ((cg & 3) == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx_stage[mx_atom_offset(rg * 8 + i, jblk)] = (uint8_t)code[i];
+        }
+        if (col_ok) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint2 b = mx_cast_row<FMT>(v[i], code[i]);
+            if (rbase + i < rows) *reinterpret_cast<uint2 *>(p.q + (rbase + i) * cols + cbase) = b;
+          }
+        }
+      }
+      if (p.q_t != nullptr) {
+        // 32x1 column blocks: rows 32 t .. 32 t + 31 of the tile belong to
+        // warps 2 t and 2 t + 1 (both half-warps of each)
+        uint32_t colmax[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          colmax[j] = Row8<InT>::colmax_bits(cmp, j);
+          colmax[j] = max(colmax[j], __shfl_xor_sync(0xFFFFFFFFu, colmax[j], 16));
+        }
+        if (lane < 16) {
+          *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8]) =
+              make_uint4(colmax[0], colmax[1], colmax[2], colmax[3]);
+          *reinterpret_cast<uint4 *>(&sh_colmax[warp][cg * 8 + 4]) =
+              make_uint4(colmax[4], colmax[5], colmax[6], colmax[7]);
+        }
+        __syncthreads();
+        const int wpair = warp & ~1;
+        uint32_t ccode[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          ccode[j] = mx_code<FMT>(max(sh_colmax[wpair][cg * 8 + j], sh_colmax[wpair + 1][cg * 8 + j]));
+        if ((warp & 1) == 0 && lane < 16) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            mx_stage[512 + mx_atom_offset(cg * 8 + j, warp >> 1)] = (uint8_t)ccode[j];
+        }
+        uint2 cb[8];
+        const bool valid = col_ok && rchunk_ok;
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float cv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) cv[i] = v[i].at(j);
+            cb[j] = mx_cast8<FMT>(cv, ccode[j]);
+          }
+        }
+        store_qt(cb, valid, r0, c0);
+      }
+      __syncthreads();   // the tile's atoms are complete
+      if (p.q != nullptr && tid < 32)
+        reinterpret_cast<uint4 *>(p.mx_scales + ((int64_t)tr * tiles_c + tc) * 512)[tid] =
+            reinterpret_cast<const uint4 *>(mx_stage)[tid];
+      if (p.q_t != nullptr && tid >= 32 && tid < 64)
+        reinterpret_cast<uint4 *>(p.mxt_scales + ((int64_t)tc * tiles_r + tr) * 512)[tid - 32] =
+            reinterpret_cast<const uint4 *>(mx_stage + 512)[tid - 32];
+    }
+
     // Shared scratch that crosses warps is reused by the next tile.  Per-tensor,
     // delayed and 1x128 row-tile casts keep theirs per warp (ordered by the
     // barrier at the top of the next iteration).
@@ -987,6 +1148,8 @@ cudaError_t dispatch_mode(const QuantParams &p, cudaStream_t stream) {
       return launch_variant<InT, FMT, kKRowCast>(p, stream);
     case kModeTensorFused:
       return launch_variant<InT, FMT, kKTensorFused>(p, stream);
+    case kModeMx:
+      return launch_variant<InT, FMT, kKMx>(p, stream);
     case kModeTile:
       if (p.q != nullptr && p.q_t != nullptr) return launch_variant<InT, FMT, kKTileBoth>(p, stream);
       if (p.q != nullptr) return launch_variant<InT, FMT, kKTileRow>(p, stream);

@@ -204,21 +204,26 @@ def test_gemm_exact_when_sums_are_exact(fq):
 
 
 def test_gemm_scale_selects_each_block(fq):
-    """One nonzero scale block per row: with A's codes all 1.0 and B's all 1.0,
-    C[m, n] = 32 * 2^(sa[m, j] - 127) * 2^(sb[n, j] - 127) summed over the
-    blocks -- a closed form that pins which scale byte each K step uses."""
-    M, N, K = 128, 256, 512
+    """A's and B's codes all 1.0, a different scale per row and 32-wide block:
+    C[m, n] = 32 * sum_j 2^(sa[m, j] - 127) * 2^(sb[n, j] - 127), a closed
+    form that pins which scale byte (and which tensor-memory column and lane)
+    every K step uses.  Codes stay within 125..129, so every term is a
+    multiple of 2^-3 and the sums are exact in fp32: the result must equal the
+    closed form bit for bit.  (With terms spread over 2^25 the tensor cores'
+    accumulator, which drops addends below the running sum's last place, can
+    land 2.3e-6 low on such an all-positive sum.)"""
+    M, N, K = 128, 512, 512
     A = np.full((M, K), 0x38, np.uint8)
     B = np.full((N, K), 0x38, np.uint8)
     rng = np.random.default_rng(12)
-    sa = rng.integers(120, 134, (M, K // 32)).astype(np.uint8)
-    sb = rng.integers(120, 134, (N, K // 32)).astype(np.uint8)
+    sa = rng.integers(125, 130, (M, K // 32)).astype(np.uint8)
+    sb = rng.integers(125, 130, (N, K // 32)).astype(np.uint8)
     opA, opB = gemm_host_operands(fq, A, sa, B, sb, 0, 0)
     y = f32(fq.fp8_gemm(opA, opB, out_dtype=torch.float32)).astype(np.float64)
     ea = np.ldexp(1.0, sa.astype(np.int64) - 127)
     eb = np.ldexp(1.0, sb.astype(np.int64) - 127)
     closed = 32.0 * ea @ eb.T
-    assert np.allclose(y, closed, rtol=1e-6, atol=0)
+    assert np.array_equal(y, closed)
 
 
 @pytest.mark.parametrize("layer", [1, 3])   # attention out (4096x4096), MLP down (K = 16384)

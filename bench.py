@@ -70,7 +70,15 @@ PROFILE_CASES = {
     "amax": "16384x8192 bf16 amax",
     "quant_activation": ("the bench's 8192x4096 activation, 1x128 row tiles, E4M3, L2 flushed "
                          "before each of the three calls"),
+    "quant_mx_dual": "16384x8192 bf16, MXFP8 1x32 row and 32x1 column blocks, E4M3",
+    "gemm_mx": "8192x8192x8192 MXFP8 x MXFP8 GEMM, bf16 out",
 }
+# One linear of the layer, its Fprop, Dgrad and Wgrad once each (three GEMM
+# launches after the quantisation): layer_<recipe>_<linear>.
+for _rc in ("tensor", "block", "mx"):
+    for _ln in ("qkv", "attn_out", "mlp_up", "mlp_down"):
+        PROFILE_CASES[f"layer_{_rc}_{_ln}"] = (f"the layer's {_ln} Fprop, Dgrad and Wgrad, "
+                                               f"{_rc} scaling, bf16 out")
 
 
 def run_profile_case(case: str):
@@ -80,7 +88,42 @@ def run_profile_case(case: str):
     import workloads
     build_lib.build()
     fq.load_library()
-    if case.startswith("gemm"):
+    if case.startswith("layer_"):
+        recipe, name = case[len("layer_"):].split("_", 1)
+        idx = [s.name for s in workloads.LAYER].index(name)
+        x, w, g = (t.cuda() for t in workloads.layer_inputs(workloads.LAYER[idx], idx))
+        if recipe == "tensor":
+            qx, qxt, sx = fq.fp8_quantize_tensor(x, fq.E4M3, fq.fp8_amax(x), want_qt=True)
+            qw, qwt, sw = fq.fp8_quantize_tensor(w, fq.E4M3, fq.fp8_amax(w), want_qt=True)
+            qg, qgt, sg = fq.fp8_quantize_tensor(g, fq.E5M2, fq.fp8_amax(g), want_qt=True)
+            T = fq.GemmOperand.tensor
+            ops = [(fq.fp8_gemm_fprop, T(qx, 0, sx), T(qw, 0, sw)),
+                   (fq.fp8_gemm_dgrad, T(qg, 1, sg), T(qwt, 0, sw)),
+                   (fq.fp8_gemm_wgrad, T(qgt, 1, sg), T(qxt, 0, sx))]
+        elif recipe == "block":
+            qx, sx, qxt, sxt = fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True, cols=True)
+            qw, qwt, sw = fq.fp8_quantize_block128x128(w, fq.E4M3, want_q=True, want_qt=True)
+            qg, sg, qgt, sgt = fq.fp8_quantize_tile1x128(g, fq.E5M2, rows=True, cols=True)
+            T, B, BT = fq.GemmOperand.tile, fq.GemmOperand.block, fq.GemmOperand.block_transposed
+            ops = [(fq.fp8_gemm_fprop, T(qx, 0, sx), B(qw, 0, sw)),
+                   (fq.fp8_gemm_dgrad, T(qg, 1, sg), BT(qwt, 0, sw)),
+                   (fq.fp8_gemm_wgrad, T(qgt, 1, sgt), T(qxt, 0, sxt))]
+        else:
+            qx, sx, qxt, sxt = fq.fp8_quantize_mxfp8(x, fq.E4M3, rows=True, cols=True)
+            qw, sw, qwt, swt = fq.fp8_quantize_mxfp8(w, fq.E4M3, rows=True, cols=True)
+            qg, sg, qgt, sgt = fq.fp8_quantize_mxfp8(g, fq.E5M2, rows=True, cols=True)
+            X = fq.GemmOperand.mx
+            ops = [(fq.fp8_gemm_fprop, X(qx, 0, sx), X(qw, 0, sw)),
+                   (fq.fp8_gemm_dgrad, X(qg, 1, sg), X(qwt, 0, swt)),
+                   (fq.fp8_gemm_wgrad, X(qgt, 1, sgt), X(qxt, 0, sxt))]
+        del x, w, g
+        for fn, A, B in ops:
+            fn(A, B)
+    elif case == "quant_mx_dual":
+        x = workloads.normal((16384, 8192), 1.0, 902).cuda()
+        for _ in range(3):
+            fq.fp8_quantize_mxfp8(x, fq.E4M3, rows=True, cols=True)
+    elif case.startswith("gemm"):
         M = N = K = 8192
         a = workloads.normal((M, K), 1.0, 900).cuda()
         b = workloads.normal((N, K), 0.02, 901).cuda()
@@ -88,6 +131,10 @@ def run_profile_case(case: str):
             qa, _, sa = fq.fp8_quantize_tensor(a, fq.E4M3, fq.fp8_amax(a))
             qb, _, sb = fq.fp8_quantize_tensor(b, fq.E4M3, fq.fp8_amax(b))
             A, B = fq.GemmOperand.tensor(qa, 0, sa), fq.GemmOperand.tensor(qb, 0, sb)
+        elif case == "gemm_mx":
+            qa, sa, _, _ = fq.fp8_quantize_mxfp8(a, fq.E4M3)
+            qb, sb, _, _ = fq.fp8_quantize_mxfp8(b, fq.E4M3)
+            A, B = fq.GemmOperand.mx(qa, 0, sa), fq.GemmOperand.mx(qb, 0, sb)
         elif case == "gemm_row":
             qa, sa, _, _ = fq.fp8_quantize_rowwise(a, fq.E4M3)
             qb, sb, _, _ = fq.fp8_quantize_rowwise(b, fq.E4M3)
@@ -319,6 +366,11 @@ class LayerState:
             # per-tensor recipe scalars
             for nm in ("ax", "aw", "ag", "tx", "tw", "tg"):
                 L[nm] = e((1,), f32)
+            # MXFP8 recipe: E8M0 scale atoms of each operand, both orientations
+            nb = fq.mx_scale_bytes
+            L["mxx"], L["mxxt"] = e((nb(M, K),), u8), e((nb(K, M),), u8)
+            L["mxw"], L["mxwt"] = e((nb(N, K),), u8), e((nb(K, N),), u8)
+            L["mxg"], L["mxgt"] = e((nb(M, N),), u8), e((nb(N, M),), u8)
             # outputs
             L["y"], L["dx"], L["dw"] = e((M, N), bf16), e((M, K), bf16), e((N, K), bf16)
             if with_host:
@@ -362,6 +414,20 @@ class LayerState:
         return ops
 
 
+    def mx_operands(self):
+        fq = self.fq
+        X = fq.GemmOperand.mx
+        ops = []
+        for L in self.linears:
+            ops.append({
+                "fprop": (X(L["qx"], fq.E4M3, L["mxx"]), X(L["qw"], fq.E4M3, L["mxw"]), L["y"]),
+                "dgrad": (X(L["qg"], fq.E5M2, L["mxg"]), X(L["qwt"], fq.E4M3, L["mxwt"]),
+                          L["dx"]),
+                "wgrad": (X(L["qgt"], fq.E5M2, L["mxgt"]), X(L["qxt"], fq.E4M3, L["mxxt"]),
+                          L["dw"]),
+            })
+        return ops
+
     def row_operands(self):
         fq = self.fq
         R = fq.GemmOperand.row
@@ -385,10 +451,11 @@ class Runner:
         self.bops = state.block_operands()
         self.tops = state.tensor_operands()
         self.rops = state.row_operands()
-        self.gemm_events = None   # list of (start, end, flops) when recording
+        self.mops = state.mx_operands()
+        self.gemm_events = None   # list of (start, end, flops, (linear, role)) when recording
         self._cin, self._cout = self.torch.cuda.Stream(), self.torch.cuda.Stream()
 
-    def _gemm(self, role, A, B, C):
+    def _gemm(self, role, A, B, C, linear=0):
         fq, torch = self.fq, self.torch
         rec = self.gemm_events is not None
         if rec:
@@ -401,7 +468,7 @@ class Runner:
         if rec:
             e1.record(self.stream)
             M, N = C.shape
-            self.gemm_events.append((e0, e1, 2.0 * M * N * A.K))
+            self.gemm_events.append((e0, e1, 2.0 * M * N * A.K, (linear, role)))
 
     # block recipe ------------------------------------------------------
     def quantize_block(self):
@@ -417,15 +484,15 @@ class Runner:
                                       stream=st)
 
     def gemms(self, ops):
-        for o in ops:
+        for i, o in enumerate(ops):
             for role in ("fprop", "dgrad", "wgrad"):
                 A, B, C = o[role]
-                self._gemm(role, A, B, C)
+                self._gemm(role, A, B, C, i)
 
     def block_autocast(self):
         # per linear: quantise, then its three GEMMs (as autocast does)
         fq, st = self.fq, self.stream
-        for L, o in zip(self.s.linears, self.bops):
+        for i, (L, o) in enumerate(zip(self.s.linears, self.bops)):
             fq.fp8_quantize_tile1x128(L["x"], fq.E4M3, rows=True, cols=True, q=L["qx"],
                                       q_scales=L["sx"], q_t=L["qxt"], qt_scales=L["sxt"],
                                       stream=st)
@@ -435,9 +502,28 @@ class Runner:
                                       q_scales=L["sg"], q_t=L["qgt"], qt_scales=L["sgt"],
                                       stream=st)
             for role in ("fprop", "dgrad", "wgrad"):
-                self._gemm(role, *o[role])
+                self._gemm(role, *o[role], i)
 
     block_autocast.launches = 4 * 6
+
+    # MXFP8 recipe ------------------------------------------------------
+    def mx_autocast(self):
+        # per linear: x, w and grad_out each quantised once into both
+        # orientations (1x32 row blocks and 32x1 column blocks), then the
+        # three block-scaled GEMMs
+        fq, st = self.fq, self.stream
+        for i, (L, o) in enumerate(zip(self.s.linears, self.mops)):
+            for nm, fmt in (("x", fq.E4M3), ("w", fq.E4M3), ("g", fq.E5M2)):
+                fq.fp8_quantize_mxfp8(L[nm], fmt, rows=True, cols=True, q=L["q" + nm],
+                                      q_scales=L["mx" + nm], q_t=L["q" + nm + "t"],
+                                      qt_scales=L["mx" + nm + "t"], stream=st)
+            for role in ("fprop", "dgrad", "wgrad"):
+                self._gemm(role, *o[role], i)
+
+    mx_autocast.launches = 4 * 6
+
+    def mx_prequant(self):
+        self.gemms(self.mops)
 
     def block_prequant(self):
         self.gemms(self.bops)
@@ -467,7 +553,7 @@ class Runner:
                 fq.fp8_quantize_tensor(L["g"], fq.E5M2, L["ag"], want_q=True, want_qt=True,
                                        q=L["qg"], q_t=L["qgt"], scale=L["tg"], stream=st)
             for role in ("fprop", "dgrad", "wgrad"):
-                self._gemm(role, *o[role])
+                self._gemm(role, *o[role], i)
 
     tensor_autocast.launches = 4 * 9   # per linear: 3 amax, 3 casts, 3 GEMMs
 
@@ -477,13 +563,13 @@ class Runner:
     # row-wise recipe ----------------------------------------------------
     def row_autocast(self):
         fq, st = self.fq, self.stream
-        for L, o in zip(self.s.linears, self.rops):
+        for i, (L, o) in enumerate(zip(self.s.linears, self.rops)):
             for nm, fmt in (("x", fq.E4M3), ("w", fq.E4M3), ("g", fq.E5M2)):
                 fq.fp8_quantize_rowwise(L[nm], fmt, rows=True, cols=True, q=L["q" + nm],
                                         q_scales=L["r" + nm], q_t=L["q" + nm + "t"],
                                         qt_scales=L["r" + nm + "t"], stream=st)
             for role in ("fprop", "dgrad", "wgrad"):
-                self._gemm(role, *o[role])
+                self._gemm(role, *o[role], i)
 
     row_autocast.launches = 4 * 15   # per linear: 3 x (2 quantize passes + 2 finalizes), 3 GEMMs
 
@@ -523,7 +609,7 @@ class Runner:
                                        q=L["q" + k], q_t=L["q" + k + "t"], scale=L["t" + k],
                                        stream=st)
             for role, out in (("fprop", "y"), ("dgrad", "dx"), ("wgrad", "dw")):
-                self._gemm(role, *o[role])
+                self._gemm(role, *o[role], i)
                 done = torch.cuda.Event()
                 done.record(st)
                 self._cout.wait_event(done)
@@ -621,14 +707,20 @@ def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None, 
 # ------------------------------------------------------------- CPU baseline
 
 class OracleLayerSample:
-    """The oracle on a bounded sample of the block-scaled layer step: for
-    each of the 12 GEMMs, `rows` output rows x one 128-row block of B.  The
-    inputs are drawn once; each run() quantises those A rows and that B block
-    with the oracle (1x128 tiles / 128x128 blocks) and computes the
-    double-accumulated GEMM, spread over `threads` host threads (the oracle is
-    plain C; ctypes releases the GIL).  run() returns (flops, seconds)."""
+    """The oracle on a bounded sample of the headline step (per-tensor current
+    scaling, E4M3 x and w, E5M2 grad_out): every run() takes, for each of the
+    four linears, the amax of ALL of x, w and grad_out (the recipe's scale
+    needs the whole tensor; the oracle's amax runs over row chunks on the
+    host threads, and a max is exact in any order), their scales, then for
+    each of the 12 GEMMs casts `rows` rows of A and one 128-row block of B with
+    those scales and forms that rows x 128 block of the output in double.
+    ctypes releases the GIL, so the plain-C oracle runs on `threads` host
+    threads.  run() returns (GEMM flops of the sample, seconds)."""
 
-    def __init__(self, rows: int, threads: int):
+    ROWS = 64     # one sample size for the reference arm and cpu_baseline
+    BROWS = 64
+
+    def __init__(self, threads: int, rows: int = ROWS, brows: int = BROWS):
         import numpy as np
         import torch
 
@@ -637,45 +729,57 @@ class OracleLayerSample:
         def bits(t):
             return np.ascontiguousarray(t.contiguous().view(torch.int16).numpy().view(np.uint16))
 
-        self.rows, self.threads = rows, threads
-        self.jobs = []
+        self.rows, self.brows, self.threads = rows, brows, threads
+        self.linears = []
         for i, shape in enumerate(workloads.LAYER):
             x, w, g = workloads.layer_inputs(shape, i)
-            # fprop: A = x rows (1x128), B = w rows 0..127 (block)
-            self.jobs.append((bits(x[:rows]), bits(w[:128]), 0, 0, "block"))
-            # dgrad: A = g rows (1x128, E5M2), B = rows 0..127 of w^T (block)
-            self.jobs.append((bits(g[:rows]), bits(w[:, :128].t()), 1, 0, "block"))
-            # wgrad: A = rows of g^T (column tiles of g), B = rows of x^T
-            self.jobs.append((bits(g[:, :rows].t()), bits(x[:, :128].t()), 1, 0, "tile"))
+            xb, wb, gb = bits(x), bits(w), bits(g)
+            self.linears.append({
+                "full": (xb, wb, gb),
+                # (A rows, A format, A scale source, B rows, B format, B scale source)
+                "jobs": [
+                    (xb[:rows], 0, 0, wb[:brows], 0, 1),                             # fprop
+                    (gb[:rows], 1, 2, np.ascontiguousarray(wb[:, :brows].T), 0, 1),   # dgrad
+                    (np.ascontiguousarray(gb[:, :rows].T), 1, 2,
+                     np.ascontiguousarray(xb[:, :brows].T), 0, 0),                  # wgrad
+                ]})
+
+    def description(self) -> str:
+        return (f"per-tensor current scaling of the 15872-token layer: amax of all of x, w and "
+                f"grad_out of the four linears, then for each of the 12 GEMMs the cast of "
+                f"{self.rows} rows of A and {self.brows} rows of B and their {self.rows} x "
+                f"{self.brows} output block in double, per step")
 
     def run(self):
         import concurrent.futures as cf
 
+        import numpy as np
+
         import oracle
 
-        pool = cf.ThreadPoolExecutor(max_workers=self.threads)
-
-        def one(job):
-            a, b, fa, fb, bkind = job
-            qa, sa = oracle.quantize_tile_rows(a, fa)
-            A = oracle.GemmOperand.tile(qa, fa, sa)
-            if bkind == "block":
-                qb, _, sb = oracle.quantize_block(b, fb)
-                B = oracle.GemmOperand.block(qb, fb, sb)
-            else:
-                qb, sb = oracle.quantize_tile_rows(b, fb)
-                B = oracle.GemmOperand.tile(qb, fb, sb)
-            step = max(1, a.shape[0] // 8)
-            parts = [(m0, min(a.shape[0], m0 + step)) for m0 in range(0, a.shape[0], step)]
-            list(pool.map(lambda pr: oracle.gemm_rows(A, B, pr[0], pr[1]), parts))
-            return 2.0 * a.shape[0] * b.shape[0] * a.shape[1]
-
         t0 = time.perf_counter()
-        with cf.ThreadPoolExecutor(max_workers=max(1, self.threads // 8)) as outer:
-            flops = sum(outer.map(one, self.jobs))
-        dt = time.perf_counter() - t0
-        pool.shutdown()
-        return flops, dt
+        with cf.ThreadPoolExecutor(max_workers=self.threads) as pool:
+            def amax_all(arr):
+                step = max(1, arr.shape[0] // self.threads)
+                parts = [arr[r:r + step] for r in range(0, arr.shape[0], step)]
+                return max(pool.map(lambda a: float(oracle.amax(a)), parts))
+
+            flops = 0.0
+            for L in self.linears:
+                xb, wb, gb = L["full"]
+                amx = [amax_all(xb), amax_all(wb), amax_all(gb)]
+                fmts = [0, 0, 1]
+                sc = [oracle.scale_from_amax(a, f) for a, f in zip(amx, fmts)]
+                for a, fa, ia, b, fb, ib in L["jobs"]:
+                    qa, _, _ = oracle.quantize_tensor(a, fa, sc[ia])
+                    qb, _, _ = oracle.quantize_tensor(b, fb, sc[ib])
+                    A = oracle.GemmOperand.tensor(qa, fa, sc[ia])
+                    B = oracle.GemmOperand.tensor(qb, fb, sc[ib])
+                    step = max(1, a.shape[0] // self.threads)
+                    parts = [(m0, min(a.shape[0], m0 + step)) for m0 in range(0, a.shape[0], step)]
+                    list(pool.map(lambda pr: oracle.gemm_rows(A, B, pr[0], pr[1]), parts))
+                    flops += 2.0 * a.shape[0] * b.shape[0] * a.shape[1]
+        return flops, time.perf_counter() - t0
 
 
 def cpu_cores():
@@ -689,14 +793,13 @@ def cpu_cores():
 
 def run_reference(args, dist):
     """The oracle as the reference arm: each step is the bounded sample of
-    the layer step above, timed on the host cores."""
+    the headline step above, timed on the host cores."""
     if dist.rank != 0:
         return
     import oracle
     oracle.build()
     threads = cpu_cores()
-    rows = 128
-    sample_run = OracleLayerSample(rows, threads)
+    sample_run = OracleLayerSample(threads)
     for _ in range(args.warmup):
         sample_run.run()
     flops = secs = 0.0
@@ -705,8 +808,6 @@ def run_reference(args, dist):
         flops += f
         secs += s
     tflops = flops / secs / 1e12
-    sample = (f"{rows} output rows x 128 columns of each of the 12 layer GEMMs (A rows and one "
-              f"128-row B block quantised by the oracle, then double-accumulated), per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -714,7 +815,7 @@ def run_reference(args, dist):
         "vs_baseline": None, "dtype": "fp8->f64", "data": "synthetic",
         "config": layer_config(),
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample_run.description()},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -733,6 +834,66 @@ def layer_config():
         "out_dtype": "bf16",
         "l2": "inputs larger than L2 (each step streams ~5 GB of operands)",
     }
+
+
+def tiny_linear_latency(fq, torch, stream, reps: int = 200):
+    """The fp8_parity page's linear (x 512x32, w 64x32, grad_out 512x64, fp32,
+    per-tensor current scaling, fp32 outputs): microseconds per call of each
+    GEMM (operands quantised beforehand) and of the whole autocast forward +
+    backward (amax, cast with the transposed copy and the three GEMMs), as
+    `reps` back-to-back launches on one stream timed with CUDA events.  At
+    2 MFLOP per GEMM this is launch latency, not a roofline."""
+    import workloads
+    x, w, g = (t.cuda() for t in workloads.tiny_linear())
+    f32 = torch.float32
+    e = lambda shp, dt: torch.empty(shp, dtype=dt, device=x.device)
+    q = {k: (e(t.shape, torch.uint8), e(t.shape[::-1], torch.uint8), e((1,), f32), e((1,), f32))
+         for k, t in (("x", x), ("w", w), ("g", g))}
+    src = {"x": x, "w": w, "g": g}
+    fmt = {"x": fq.E4M3, "w": fq.E4M3, "g": fq.E5M2}
+    y, dx, dw = e((512, 64), f32), e((512, 32), f32), e((64, 32), f32)
+
+    def quantize():
+        for k in "xwg":
+            qq, qt, am, sc = q[k]
+            fq.fp8_amax(src[k], out=am, stream=stream)
+            fq.fp8_quantize_tensor(src[k], fmt[k], am, want_q=True, want_qt=True, q=qq, q_t=qt,
+                                   scale=sc, stream=stream)
+
+    T = fq.GemmOperand.tensor
+    gemm = {
+        "fprop_512x64x32": lambda: fq.fp8_gemm_fprop(T(q["x"][0], 0, q["x"][3]),
+                                                     T(q["w"][0], 0, q["w"][3]), out=y,
+                                                     stream=stream),
+        "dgrad_512x32x64": lambda: fq.fp8_gemm_dgrad(T(q["g"][0], 1, q["g"][3]),
+                                                     T(q["w"][1], 0, q["w"][3]), out=dx,
+                                                     stream=stream),
+        "wgrad_64x32x512": lambda: fq.fp8_gemm_wgrad(T(q["g"][1], 1, q["g"][3]),
+                                                     T(q["x"][1], 0, q["x"][3]), out=dw,
+                                                     stream=stream),
+    }
+
+    def per_call_us(fn):
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1e3
+
+    quantize()
+    out = {k: round(per_call_us(fn), 2) for k, fn in gemm.items()}
+    out["quantize_x_w_g_us"] = round(per_call_us(quantize), 2)
+    out["autocast_fwd_bwd_us"] = round(per_call_us(lambda: (quantize(), [fn() for fn in
+                                                                       gemm.values()])), 2)
+    out["note"] = ("us per call, back-to-back on one stream (CUDA events over "
+                   f"{reps} calls); the autocast step is 3 amax + 3 casts + 3 GEMMs = 9 launches")
+    return out
 
 
 # --------------------------------------------------------------------- main
@@ -779,34 +940,67 @@ def main():
     torch.cuda.synchronize()
     flops = state.flops
 
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fp8_peak_sust = FP8_PER_BF16 * float(peaks.get("bf16_tflops_sustained",
+                                                   FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    fp8_peak_burst = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
     def gemm_summary(events):
-        ms = sum(a.elapsed_time(b) for a, b, _ in events)
-        fl = sum(f for _, _, f in events)
+        ms = sum(a.elapsed_time(b) for a, b, _, _ in events)
+        fl = sum(f for _, _, f, _ in events)
         return ms, fl, len(events)
+
+    def gemm_table(events):
+        """Per GEMM of the layer (linear.role): mean event-timed duration over
+        the timed steps, its TFLOP/s and fraction of the burst FP8 peak."""
+        agg = {}
+        for a, b, fl, key in events:
+            t = agg.setdefault(key, [0.0, 0, fl])
+            t[0] += a.elapsed_time(b)
+            t[1] += 1
+        rows = {}
+        for (i, role), (ms, n, fl) in sorted(agg.items()):
+            us = ms / n * 1e3
+            tfl = fl / (us * 1e-6) / 1e12
+            M, N, Kc = [(m, nn, k) for nm, r, m, nn, k in workloads.gemm_problems()
+                        if nm == workloads.LAYER[i].name and r == role][0]
+            rows[f"{workloads.LAYER[i].name}.{role}"] = {
+                "MxNxK": f"{M}x{N}x{Kc}", "us": round(us, 2), "TFLOP/s": round(tfl, 1),
+                "frac": round(tfl / fp8_peak_burst, 3)}
+        return rows
+
+    per_gemm = {}
+
+    def timed(name, fn, record=True):
+        """The phase's ms per step; its per-GEMM table goes to per_gemm[name]."""
+        ms = time_steps(torch, dist, stream, fn, K, W, record=run if record else None, clk=clk)
+        out = None
+        if record and run.gemm_events:
+            per_gemm[name] = gemm_table(run.gemm_events)
+            out = gemm_summary(run.gemm_events)
+        run.gemm_events = None
+        return ms, out
 
     # ---- headline: the layer with per-tensor current scaling, autocast;
     # clocks are sampled through every timed layer phase
     with ClockSampler(uuid) as clk:
-        ms_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(False), K, W,
-                             record=run, clk=clk)
-        t_gemm_ms, t_gemm_fl, t_gemm_n = gemm_summary(run.gemm_events)
-        run.gemm_events = None
-        ms_pre = time_steps(torch, dist, stream, run.tensor_prequant, K, W, clk=clk)
-        ms_d_auto = time_steps(torch, dist, stream, lambda: run.tensor_autocast(True), K, W,
-                               clk=clk)
+        ms_auto, (t_gemm_ms, t_gemm_fl, t_gemm_n) = timed(
+            "tensor_current.autocast", lambda: run.tensor_autocast(False))
+        ms_pre, _ = timed("tensor_current.prequant", run.tensor_prequant)
+        ms_d_auto, _ = timed("tensor_delayed_grad.autocast", lambda: run.tensor_autocast(True))
 
         # ---- the same layer with 1x128 / 128x128 scaling
-        ms_b_auto = time_steps(torch, dist, stream, run.block_autocast, K, W, record=run,
-                               clk=clk)
-        b_gemm_ms, b_gemm_fl, b_gemm_n = gemm_summary(run.gemm_events)
-        run.gemm_events = None
-        ms_b_pre = time_steps(torch, dist, stream, run.block_prequant, K, W, clk=clk)
+        ms_b_auto, _ = timed("block_1x128_128x128.autocast", run.block_autocast)
+        ms_b_pre, (b_gemm_ms, b_gemm_fl, b_gemm_n) = timed("block_1x128_128x128.prequant",
+                                                           run.block_prequant)
+
+        # ---- the same layer with MXFP8 (1x32 blocks, E8M0 scales)
+        ms_m_auto, _ = timed("mxfp8.autocast", run.mx_autocast)
+        ms_m_pre, (m_gemm_ms, m_gemm_fl, m_gemm_n) = timed("mxfp8.prequant", run.mx_prequant)
 
         # ---- the same layer with row-wise scaling
-        ms_r_auto = time_steps(torch, dist, stream, run.row_autocast, K, W, record=run, clk=clk)
-        r_gemm_ms, r_gemm_fl, r_gemm_n = gemm_summary(run.gemm_events)
-        run.gemm_events = None
-        ms_r_pre = time_steps(torch, dist, stream, run.row_prequant, K, W, clk=clk)
+        ms_r_auto, _ = timed("rowwise.autocast", run.row_autocast)
+        ms_r_pre, (r_gemm_ms, r_gemm_fl, r_gemm_n) = timed("rowwise.prequant", run.row_prequant)
 
         # ---- amax fused into the GEMM that produces the next quantize's input:
         # QKV Fprop alone, followed by a separate amax of y, and with the fused amax
@@ -903,24 +1097,25 @@ def main():
         import oracle
         oracle.build()
         threads = cpu_cores()
-        rows = 512
-        f, s = OracleLayerSample(rows, threads).run()
+        sample_run = OracleLayerSample(threads)
+        f = s = 0.0
+        reps = 0
+        while s < 10.0 and reps < 20:     # about ten seconds of host work
+            df, ds = sample_run.run()
+            f, s, reps = f + df, s + ds, reps + 1
         cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": (f"{rows} output rows x 128 columns of each of the 12 layer GEMMs "
-                          f"(oracle quantises those A rows and one 128-row B block, then "
-                          f"double-accumulates); {f / 1e9:.2f} GFLOP in {s:.1f} s")}
+               "sample": (f"{sample_run.description()}; {reps} steps, {f / 1e9:.2f} GFLOP "
+                          f"in {s:.1f} s")}
 
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    fp8_peak_sust = FP8_PER_BF16 * float(peaks.get("bf16_tflops_sustained",
-                                                   FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    fp8_peak_burst = FP8_PER_BF16 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     t_gemm_tflops = t_gemm_fl / (t_gemm_ms * 1e-3) / 1e12
     b_gemm_tflops = b_gemm_fl / (b_gemm_ms * 1e-3) / 1e12
+    m_gemm_tflops = m_gemm_fl / (m_gemm_ms * 1e-3) / 1e12
     r_gemm_tflops = r_gemm_fl / (r_gemm_ms * 1e-3) / 1e12
     tile_gbps = gbps(tile_bytes, ms_tile)
     tf = lambda ms: flops / (ms * 1e-3) / 1e12
-    peak_src = (f"{peak_src}: bf16_tflops_sustained x {FP8_PER_BF16} (dense FP8/BF16 nominal "
-                "ratio)")
+    peak_src = (f"{peak_src}: bf16_tflops (burst: the layer step is {ms_auto:.1f} ms, not a "
+                f"seconds-long loop) x {FP8_PER_BF16} (dense FP8/BF16 nominal ratio)")
+    tiny = tiny_linear_latency(fq, torch, stream)
 
     line = {
         "metric": METRIC,
@@ -947,18 +1142,30 @@ def main():
             "autocast": {"value": tf(ms_b_auto), "ms_per_step": ms_b_auto},
             "prequant": {"value": tf(ms_b_pre), "ms_per_step": ms_b_pre},
             "unit": "TFLOP/s",
-            "roofline": {"bound": "tensor", "achieved": b_gemm_tflops, "peak": fp8_peak_sust,
-                         "unit": "TFLOP/s", "frac": b_gemm_tflops / fp8_peak_sust,
+            "roofline": {"bound": "tensor", "achieved": b_gemm_tflops, "peak": fp8_peak_burst,
+                         "unit": "TFLOP/s", "frac": b_gemm_tflops / fp8_peak_burst,
                          "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_blockscaled_kernel"),
-                         "kernel": "gemm_blockscaled_kernel",
+                         "kernel": "gemm_blockscaled_kernel (prequant step)",
                          "launches": b_gemm_n}},
+        "mxfp8": {
+            "workload": ("the same 12 GEMMs with MXFP8 (OCP MX v1.0: 1x32 blocks, E8M0 scales) "
+                         "on x, w and grad_out, each quantised into both orientations"),
+            "autocast": {"value": tf(ms_m_auto), "ms_per_step": ms_m_auto},
+            "prequant": {"value": tf(ms_m_pre), "ms_per_step": ms_m_pre},
+            "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": m_gemm_tflops, "peak": fp8_peak_burst,
+                         "unit": "TFLOP/s", "frac": m_gemm_tflops / fp8_peak_burst,
+                         "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_mx_kernel"),
+                         "kernel": ("gemm_mx_kernel, tcgen05.mma kind::mxf8f6f4 block_scale "
+                                    "(prequant step)"),
+                         "launches": m_gemm_n}},
         "rowwise": {
             "workload": ("the same 12 GEMMs with one scale per row of each K-major operand "
                          "(x, w and grad_out quantised along both orientations)"),
             "autocast": {"value": tf(ms_r_auto), "ms_per_step": ms_r_auto},
             "prequant": {"value": tf(ms_r_pre), "ms_per_step": ms_r_pre},
             "unit": "TFLOP/s",
-            "gemm": {"achieved": r_gemm_tflops, "frac": r_gemm_tflops / fp8_peak_sust,
+            "gemm": {"achieved": r_gemm_tflops, "frac": r_gemm_tflops / fp8_peak_burst,
                      "kernel": "gemm_tensor_pair_kernel (cta_group::2), row-scale epilogue",
                      "launches": r_gemm_n}},
         "fused_amax": {
@@ -970,6 +1177,7 @@ def main():
         "context_pages_B300_ms_per_layer": {
             "fp8_current_autocast": 9.15, "fp8_current_prequant": 6.81,
             "fp8_delayed_autocast": 7.80, "mxfp8_autocast": 8.98,
+            "fp8_delayed_prequant_reported": 8.12,
             "note": ("the blog repost's CodonFM-5B layer on B300 with Transformer Engine; "
                      "context, not the target")},
         "quantize": {
@@ -1002,12 +1210,15 @@ def main():
                          "note": "dequantised E4M3 vs the bf16 input; 1x128 tiles should be lower"},
             "unit": "GB/s", "peak": hbm_peak,
         },
-        "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_sust,
-                     "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_sust,
+        "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_burst,
+                     "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_burst,
                      "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_tensor_pair_kernel"),
                      "kernel": "gemm_tensor_pair_kernel, cta_group::2 (12 GEMMs of the autocast step)",
                      "launches": t_gemm_n, "peak_source": peak_src,
-                     "frac_of_burst": t_gemm_tflops / fp8_peak_burst},
+                     "frac_of_sustained": t_gemm_tflops / fp8_peak_sust},
+        "per_gemm": dict(per_gemm, unit="us per launch (CUDA events inside the timed steps)",
+                         peak_tflops=fp8_peak_burst),
+        "tiny_linear": tiny,
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,
                               "unit": "GB/s", "frac": tile_gbps / hbm_peak,
                               "traffic": recorded_traffic("fp8q_quant.cu", "quant2d_tile_rows"),

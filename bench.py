@@ -180,18 +180,33 @@ def run_profile_case(case: str):
     print(f"profile case {case} done: {PROFILE_CASES[case]}")
 
 
-def recorded_traffic(kernel_file: str, key: str):
-    """DRAM bytes per launch for a kernel, from profiles/roofline_traffic.json,
-    only if the kernel's source is unchanged since that capture (its sha256
-    is stored with the figure); otherwise None."""
+KERNEL_SOURCES = {
+    "gemm_tensor_pair_kernel": ("fp8q_gemm.cu", "fp8q_gemm_common.cuh", "fp8q_ptx.cuh"),
+    "gemm_blockscaled_kernel": ("fp8q_gemm_block.cu", "fp8q_gemm_common.cuh", "fp8q_ptx.cuh"),
+    "gemm_mx_kernel": ("fp8q_gemm_mx.cu", "fp8q_gemm_common.cuh", "fp8q_ptx.cuh"),
+    "quant2d_tile_rows": ("fp8q_quant.cu", "fp8q_ptx.cuh"),
+}
+
+
+def kernel_source_digest(key: str) -> str:
+    """sha256 over the source files a kernel is built from."""
     import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[key]:
+        with open(os.path.join(ROOT, "scaled_quantize_fp8_warp_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(key: str):
+    """DRAM bytes per launch for a kernel, from profiles/roofline_traffic.json,
+    only if the kernel's sources are unchanged since that capture (their
+    sha256 is stored with the figure); otherwise None."""
     path = os.path.join(ROOT, "profiles", "roofline_traffic.json")
-    src = os.path.join(ROOT, "scaled_quantize_fp8_warp_gb300", "csrc", kernel_file)
     try:
         with open(path) as f:
             rec = json.load(f).get(key)
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
+        digest = kernel_source_digest(key)
     except (OSError, ValueError):
         return None
     if not rec or rec.get("source_sha256") != digest:
@@ -1144,7 +1159,7 @@ def main():
             "unit": "TFLOP/s",
             "roofline": {"bound": "tensor", "achieved": b_gemm_tflops, "peak": fp8_peak_burst,
                          "unit": "TFLOP/s", "frac": b_gemm_tflops / fp8_peak_burst,
-                         "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_blockscaled_kernel"),
+                         "traffic": recorded_traffic("gemm_blockscaled_kernel"),
                          "kernel": "gemm_blockscaled_kernel (prequant step)",
                          "launches": b_gemm_n}},
         "mxfp8": {
@@ -1155,7 +1170,7 @@ def main():
             "unit": "TFLOP/s",
             "roofline": {"bound": "tensor", "achieved": m_gemm_tflops, "peak": fp8_peak_burst,
                          "unit": "TFLOP/s", "frac": m_gemm_tflops / fp8_peak_burst,
-                         "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_mx_kernel"),
+                         "traffic": recorded_traffic("gemm_mx_kernel"),
                          "kernel": ("gemm_mx_kernel, tcgen05.mma kind::mxf8f6f4 block_scale "
                                     "(prequant step)"),
                          "launches": m_gemm_n}},
@@ -1212,7 +1227,7 @@ def main():
         },
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_burst,
                      "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_burst,
-                     "traffic": recorded_traffic("fp8q_gemm.cu", "gemm_tensor_pair_kernel"),
+                     "traffic": recorded_traffic("gemm_tensor_pair_kernel"),
                      "kernel": "gemm_tensor_pair_kernel, cta_group::2 (12 GEMMs of the autocast step)",
                      "launches": t_gemm_n, "peak_source": peak_src,
                      "frac_of_sustained": t_gemm_tflops / fp8_peak_sust},
@@ -1221,7 +1236,7 @@ def main():
         "tiny_linear": tiny,
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,
                               "unit": "GB/s", "frac": tile_gbps / hbm_peak,
-                              "traffic": recorded_traffic("fp8q_quant.cu", "quant2d_tile_rows"),
+                              "traffic": recorded_traffic("quant2d_tile_rows"),
                               "kernel": "quant2d_kernel (1x128 row tiles)",
                               "peak_source": "measured: hbm_gbs"},
         "cpu_baseline": cpu,

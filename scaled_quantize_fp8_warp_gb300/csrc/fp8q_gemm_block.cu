@@ -1,0 +1,275 @@
+// The tile/block-scaled FP8 GEMM (1x128 tiles on A; 128x128 blocks or 1x128
+// tiles on B): each 128-wide K block is accumulated into a ping-pong TMEM
+// buffer and promoted into fp32 registers with that block's scale product
+// (the blocked sum of the definition; "fp8_parity.py", FP8Matmul, with the
+// scales applied per K block).
+#include "fp8q_gemm_common.cuh"
+
+namespace fp8q {
+namespace gemm {
+namespace {
+
+// ------------------------------------------------------------------------
+// Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0) and the MMA
+// issuer (warp 1); NWG promotion warpgroups follow, warpgroup g owning tile
+// columns [g C, g C + C) with C = BN / NWG.  A carries 1x128 tile scales; B
+// carries 128x128 block scales (B_TILE = false) or 1x128 tile scales
+// (B_TILE = true).  Each 128-wide K block is accumulated into one of two
+// TMEM buffers of BN columns; the promotion warps load their C columns of it
+// (64 per round trip), hand the buffer back, and add it into fp32 registers
+// with the block's scale product.
+//
+// Register split (setmaxnreg inside each role's branch): the launch of
+// 128 (1 + NWG) threads gets kLaunchRegs per thread; warpgroup 0 drops to
+// kLowRegs and the promotion warpgroups rise to kHighRegs, with
+// 128 kLowRegs + 128 NWG kHighRegs <= 128 (1 + NWG) kLaunchRegs.  The host
+// checks the compiled launch count before the first launch.
+// ------------------------------------------------------------------------
+template <int BN, int NWG>
+struct BSConfig {
+  static constexpr int kThreads = 128 * (1 + NWG);
+  static constexpr int kCols = BN / NWG;                 // columns per promotion warpgroup
+  static constexpr int kStages = BN <= 192 ? 5 : 4;
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr int kLowRegs = NWG == 2 ? 40 : 56;
+  static constexpr int kHighRegs = ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8 > 232
+                                       ? 232
+                                       : ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8;
+  static constexpr uint32_t kTmemCols = 512;              // two BN-column buffers fit
+  static_assert(BN % NWG == 0 && (kCols == 64 || kCols == 128), "64 or 128 columns per WG");
+  static_assert(2 * BN <= 512, "two partial-sum buffers must fit in TMEM");
+  static_assert(128 * kLowRegs + 128 * NWG * kHighRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+};
+
+template <int BN, int NWG, bool B_TILE, bool OUT_BF16>
+__global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap ta,
+                            const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
+  using Cfg = BSConfig<BN, NWG>;
+  constexpr int STAGES = Cfg::kStages;
+  constexpr int C = Cfg::kCols;
+  constexpr int NPW = 4 * NWG;   // promotion warps
+  using L = Layout<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(16) float sh_bscale[NPW][C];  // per promotion warp: B tile scales
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  const uint32_t bars = ring + L::kRingBytes;
+  const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
+  const uint32_t pf0 = bars + 8 * (2 * STAGES), pe0 = pf0 + 16;
+  const uint32_t drain = pe0 + 16;
+  const uint32_t slot = bars + L::kBarBytes;
+  uint8_t *slot_ptr = smem_raw + (slot - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(pf0 + 8 * b, 1);
+      mbar_init(pe0 + 8 * b, NPW);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    prefetch_tmap(&ta);
+    prefetch_tmap(&tb);
+  }
+  if (warp == 1) {
+    tmem_alloc(slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
+  const int total = p.num_m_tiles * p.num_n_tiles;
+  const int nkb = p.num_k_blocks;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kLowRegs));
+    if (warp == 0) {
+      if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+            if (!wait_bounded(pe0 + 8 * pb, pph ^ 1u, abort_flag, p.err) ||
+                !wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
+            mma_commit(empty0 + 8 * s);
+            mma_commit(pf0 + 8 * pb);
+          }
+        }
+        drain_mma(drain, abort_flag);
+      }
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kHighRegs));
+    const int pw = warp - 4;              // promotion warp 0 .. NPW-1
+    const int wg = pw >> 2;
+    const int quarter = warp & 3;         // TMEM lane quarter of this warp
+    float *my_bs = sh_bscale[pw];
+    constexpr int kPerLane = C / 32;      // B tile scales each lane stages (2 or 4)
+    uint32_t it = 0, run_max = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int mt, nt;
+      tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt, kBlockGroupM, 0);
+      const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
+      const bool m_ok = m < p.M;
+      const int64_t ncol0 = (int64_t)nt * BN + wg * C;   // first column of this warpgroup
+      const int64_t nl = ncol0 + lane * kPerLane;         // this lane's B-scale columns
+      auto load_sa = [&](int kb) -> float {
+        return m_ok ? p.scale_a[kb * p.a_stride_k + m * p.a_stride_row] : 0.0f;
+      };
+      // Block scales: a warpgroup's C columns may straddle two 128-column
+      // blocks when C = 64 only if ncol0 % 128 == 64; both halves of a
+      // 64-column group lie in one block, so one scale serves the group.
+      auto load_sb = [&](int kb) -> float {
+        return ncol0 < p.N ? p.scale_b[(ncol0 / 128) * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
+      };
+      float acc[C];
+#pragma unroll
+      for (int j = 0; j < C; ++j) acc[j] = 0.0f;
+      float sa_next = load_sa(0);
+      float sb_next = B_TILE ? 0.0f : load_sb(0);
+      float sbt_next[kPerLane];
+      if (B_TILE) {
+#pragma unroll
+        for (int u = 0; u < kPerLane; ++u)
+          sbt_next[u] = (nl + u < p.N) ? p.scale_b[(nl + u) * p.b_stride_row] : 0.0f;
+      }
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const float sa = sa_next;
+        const float sb = sb_next;
+        if (B_TILE) {
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < kPerLane; ++u) my_bs[lane * kPerLane + u] = sbt_next[u];
+          __syncwarp();
+        }
+        if (kb + 1 < nkb) {
+          sa_next = load_sa(kb + 1);
+          if (B_TILE) {
+#pragma unroll
+            for (int u = 0; u < kPerLane; ++u)
+              sbt_next[u] = (nl + u < p.N)
+                                ? p.scale_b[(kb + 1) * p.b_stride_k + (nl + u) * p.b_stride_row]
+                                : 0.0f;
+          } else {
+            sb_next = load_sb(kb + 1);
+          }
+        }
+        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
+        if (!wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float sab = __fmul_rn(sa, sb);
+#pragma unroll
+        for (int h = 0; h < C / 64; ++h) {
+          // 64 columns per round trip: two 32-column TMEM loads, one wait
+          uint32_t r0[32], r1[32];
+          const uint32_t col = pb * BN + wg * C + h * 64;
+          const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+          tmem_ld_32x32b_x32(tmem_base + lane_base + col, r0);
+          tmem_ld_32x32b_x32(tmem_base + lane_base + col + 32, r1);
+          tmem_ld_wait();
+          if (h == C / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pe0 + 8 * pb);
+          }
+          if (B_TILE) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]),
+                                          __fmul_rn(sa, my_bs[h * 64 + j]), acc[h * 64 + j]);
+              acc[h * 64 + 32 + j] =
+                  __fmaf_rn(__uint_as_float(r1[j]), __fmul_rn(sa, my_bs[h * 64 + 32 + j]),
+                            acc[h * 64 + 32 + j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[h * 64 + j]);
+              acc[h * 64 + 32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[h * 64 + 32 + j]);
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      if (m_ok) {
+#pragma unroll
+        for (int c = 0; c < C / 32; ++c) {
+          const int64_t n0 = ncol0 + c * 32;
+          if (n0 < p.N) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
+            run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
+          }
+        }
+      }
+    }
+    publish_amax(p.amax, run_max);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, Cfg::kTmemCols);
+}
+
+template <int BN, int NWG, bool B_TILE, bool OUT_BF16>
+int run_blockscaled(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
+                    cudaStream_t stream) {
+  using Cfg = BSConfig<BN, NWG>;
+  using L = Layout<BN, Cfg::kStages>;
+  auto kernel = gemm_blockscaled_kernel<BN, NWG, B_TILE, OUT_BF16>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    // The setmaxnreg split is only safe if the kernel launches with at least
+    // kLaunchRegs registers per thread; refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (fa.numRegs < Cfg::kLaunchRegs) return FP8Q_ERR_CUDA;
+    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
+    attr_done = true;
+  }
+  kernel<<<grid, Cfg::kThreads, L::kSmemBytes, stream>>>(ta, tb, a);
+  return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+}  // namespace
+
+int run_blockscaled_family(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
+                           int grid, bool bf16, bool b_tile, cudaStream_t stream) {
+  constexpr int BBN = kBlockScaledBN, BWG = kBlockScaledWG;
+  if (b_tile)
+    return bf16 ? run_blockscaled<BBN, BWG, true, true>(ta, tb, a, grid, stream)
+                : run_blockscaled<BBN, BWG, true, false>(ta, tb, a, grid, stream);
+  return bf16 ? run_blockscaled<BBN, BWG, false, true>(ta, tb, a, grid, stream)
+              : run_blockscaled<BBN, BWG, false, false>(ta, tb, a, grid, stream);
+}
+
+}  // namespace gemm
+}  // namespace fp8q

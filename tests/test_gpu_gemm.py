@@ -267,11 +267,13 @@ def test_layer_all_roles_full_size_tensor(fq, layer):
         check_bound(f32(got)[ms, ns], yr, ab, True, f"{shape.name} {nm}")
 
 
-def test_layer_all_roles_full_size_block(fq):
-    """Attention-out layer at full size with 1x128 / 128x128 scaling: fprop,
+@pytest.mark.parametrize("idx", [1, 2, 3])     # attention out, MLP up, MLP down
+def test_layer_all_roles_full_size_block(fq, idx):
+    """A layer linear at full size with 1x128 / 128x128 scaling: fprop,
     dgrad (B = w^T, transposed block scales) and wgrad (column tiles of g and
-    x), each sampled against the oracle."""
-    idx = 1
+    x), each on 2048 sampled outputs plus three whole 128 x 128 output tiles
+    against the oracle -- MLP up and down include the 16384-deep
+    contractions (128 promoted K blocks per output)."""
     shape = workloads.LAYER[idx]
     x, w, g = workloads.layer_inputs(shape, idx)
     M, K, N = x.shape[0], shape.K, shape.N
@@ -297,7 +299,7 @@ def test_layer_all_roles_full_size_block(fq):
                          (sgt, rsgt, "sgt")]:
         assert_f32_bits_equal(f32(got), ref, nm)
     RT, RB = oracle.GemmOperand.tile, oracle.GemmOperand.block
-    rng = np.random.default_rng(9)
+    rng = np.random.default_rng(9 + idx)
     cases = [
         (y, RT(rx, 0, rsx), RB(rw, 0, rsw), M, N, "fprop"),
         (dx, RT(rg, 1, rsg), RB(rwt, 0, rsw, transposed=True), M, K, "dgrad"),
@@ -340,6 +342,56 @@ def test_linear_autocast_matches_steps(fq):
     y2 = fq.fp8_gemm_fprop(fq.GemmOperand.tensor(qx, 0, sx), fq.GemmOperand.tensor(qw, 0, sw))
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     assert hx.state()[1] == 1 and hw.state()[1] == 1
+
+
+@pytest.mark.parametrize("recipe", ["current", "delayed", "block", "mxfp8"])
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+def test_linear_autocast_vs_oracle(fq, recipe, in_dtype):
+    """fp8_linear_autocast against the oracle's own quantisation and GEMM,
+    for every recipe, over two calls in a row.  Delayed scaling: the oracle
+    runs the same two history updates, and the device history (ring, next
+    slot, last scale) must equal it bit for bit after each call."""
+    M, N, K = 400, 272, 384
+    # histories whose maxima (8.0, 0.1225) cover the data: every quotient
+    # stays below the E4M3 overflow point
+    hist0_x = [0.5 + 0.5 * i for i in range(16)]
+    hist0_w = [0.01 + 0.0075 * i for i in range(16)]
+    hx = fq.History(initial=hist0_x) if recipe == "delayed" else None
+    hw = fq.History(initial=hist0_w) if recipe == "delayed" else None
+    ohx, ohw = np.array(hist0_x, np.float32), np.array(hist0_w, np.float32)
+    onx = onw = 0
+    code = {"current": fq.RECIPE_TENSOR_CURRENT, "delayed": fq.RECIPE_TENSOR_DELAYED,
+            "block": fq.RECIPE_BLOCK, "mxfp8": fq.RECIPE_MXFP8}[recipe]
+    for call in range(2):
+        x = workloads.normal((M, K), 1.0, 80 + call, dtype=in_dtype)
+        w = workloads.normal((N, K), 0.02, 82 + call, dtype=in_dtype)
+        y = fq.fp8_linear_autocast(x.cuda(), w.cuda(), recipe=code, hist_x=hx, hist_w=hw)
+        gpu_status_ok(fq)
+        xo, wo = to_oracle(x), to_oracle(w)
+        if recipe == "current":
+            rx, _, rsx = oracle.quantize_tensor(xo, 0)
+            rw, _, rsw = oracle.quantize_tensor(wo, 0)
+            opA, opB = oracle.GemmOperand.tensor(rx, 0, rsx), oracle.GemmOperand.tensor(rw, 0, rsw)
+        elif recipe == "delayed":
+            rx, _, rsx, ohx, onx = oracle.quantize_delayed(xo, 0, ohx, onx)
+            rw, _, rsw, ohw, onw = oracle.quantize_delayed(wo, 0, ohw, onw)
+            opA, opB = oracle.GemmOperand.tensor(rx, 0, rsx), oracle.GemmOperand.tensor(rw, 0, rsw)
+            for h, oh, on, os_, nm in ((hx, ohx, onx, rsx, "x"), (hw, ohw, onw, rsw, "w")):
+                amax_ring, nxt, scale = h.state()
+                assert_f32_bits_equal(np.array(amax_ring, np.float32), oh, f"hist_{nm} ring")
+                assert nxt == on, f"hist_{nm} next"
+                assert_f32_bits_equal(np.array([scale], np.float32), np.array([os_], np.float32),
+                                      f"hist_{nm} scale")
+        elif recipe == "block":
+            rx, rsx = oracle.quantize_tile_rows(xo, 0)
+            rw, _, rsw = oracle.quantize_block(wo, 0)
+            opA, opB = oracle.GemmOperand.tile(rx, 0, rsx), oracle.GemmOperand.block(rw, 0, rsw)
+        else:
+            rx, rsx = oracle.quantize_mx_rows(xo, 0)
+            rw, rsw = oracle.quantize_mx_rows(wo, 0)
+            opA, opB = oracle.GemmOperand.mx(rx, 0, rsx), oracle.GemmOperand.mx(rw, 0, rsw)
+        yr, ab = oracle.gemm_rows(opA, opB)
+        check_bound(f32(y), yr, ab, True, f"{recipe} call {call}")
 
 
 def test_layer_dgrad_wgrad_full_size_delayed_vs_current(fq):
@@ -471,6 +523,10 @@ def _amax_operands(fq, M, N, K, kind, seed):
         qa, sa, _, _ = fq.fp8_quantize_rowwise(a, 0)
         qb, sb, _, _ = fq.fp8_quantize_rowwise(b, 0)
         return fq.GemmOperand.row(qa, 0, sa), fq.GemmOperand.row(qb, 0, sb)
+    if kind == "mx":
+        qa, sa, _, _ = fq.fp8_quantize_mxfp8(a, 0)
+        qb, sb, _, _ = fq.fp8_quantize_mxfp8(b, 0)
+        return fq.GemmOperand.mx(qa, 0, sa), fq.GemmOperand.mx(qb, 0, sb)
     qa, sa, _, _ = fq.fp8_quantize_tile1x128(a, 0)
     qb, _, sb = fq.fp8_quantize_block128x128(b, 0)
     return fq.GemmOperand.tile(qa, 0, sa), fq.GemmOperand.block(qb, 0, sb)
@@ -482,6 +538,7 @@ def _amax_operands(fq, M, N, K, kind, seed):
     (257, 128, 512, "row"),      # one-SM kernel, 128-wide tiles, row scales
     (640, 528, 384, "row"),      # CTA-pair kernel, row scales, ragged N
     (384, 272, 640, "block"),    # block-scaled kernel
+    (400, 528, 320, "mx"),       # MXFP8 kernel, ragged M and N
 ])
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
 def test_gemm_fused_amax(fq, M, N, K, kind, out_dtype):
@@ -495,7 +552,8 @@ def test_gemm_fused_amax(fq, M, N, K, kind, out_dtype):
     iv = torch.int16 if out_dtype == torch.bfloat16 else torch.int32
     assert torch.equal(y.view(iv), y2.view(iv)), "fused amax changed the GEMM output"
     assert_f32_bits_equal(f32(am), f32(ref), "fused amax")
-    assert f32(am)[0] == np.float32(y.float().abs().max().item())
+    assert_f32_bits_equal(f32(am), np.array([oracle.amax(to_oracle(y))], np.float32),
+                          "fused amax vs oracle")
 
 
 def test_gemm_fused_amax_resets_between_calls(fq):
@@ -532,3 +590,5 @@ def test_gemm_fused_amax_full_size_qkv_fprop(fq):
     ref = fq.fp8_amax(y)
     gpu_status_ok(fq)
     assert_f32_bits_equal(f32(am), f32(ref), "fused amax")
+    assert_f32_bits_equal(f32(am), np.array([oracle.amax(to_oracle(y))], np.float32),
+                          "fused amax vs oracle")

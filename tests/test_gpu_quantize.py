@@ -307,11 +307,16 @@ def test_quantize_tensor_current_matches_two_calls(fq, dtype, shape, which):
         assert_bytes_equal(u8(q), u8(q2), "q")
     if want_qt:
         assert_bytes_equal(u8(qt), u8(qt2), "q_t")
-    if shape[0] * shape[1] <= 1 << 20:
-        rq, rqt, rs = oracle.quantize_tensor(to_oracle(x), 0, want_q=want_q, want_qt=want_qt)
-        assert_f32_bits_equal(f32(sc), np.array([rs], np.float32), "oracle scale")
-        if want_q:
-            assert_bytes_equal(u8(q), rq, "oracle q")
+    # against the oracle at every size, the cooperative one-launch case
+    # (2048 x 2048 bf16, 8 MiB) and the 64 MiB activation included
+    xo = to_oracle(x)
+    assert_f32_bits_equal(f32(am), np.array([oracle.amax(xo)], np.float32), "oracle amax")
+    rq, rqt, rs = oracle.quantize_tensor(xo, 0, want_q=want_q, want_qt=want_qt)
+    assert_f32_bits_equal(f32(sc), np.array([rs], np.float32), "oracle scale")
+    if want_q:
+        assert_bytes_equal(u8(q), rq, "oracle q")
+    if want_qt:
+        assert_bytes_equal(u8(qt), rqt, "oracle q_t")
 
 
 def test_quantize_tensor_current_special_values_and_repeats(fq):

@@ -145,9 +145,9 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
       auto load_sb = [&](int kb) -> float {
         return ncol0 < p.N ? p.scale_b[(ncol0 / 128) * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
       };
-      float acc[C];
+      float2 acc2[C / 2];   // columns (2 j, 2 j + 1)
 #pragma unroll
-      for (int j = 0; j < C; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < C / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
       float sa_next = load_sa(0);
       float sb_next = B_TILE ? 0.0f : load_sb(0);
       float sbt_next[kPerLane];
@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
         }
         tc_fence_after();
         const float sab = __fmul_rn(sa, sb);
+        const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
         for (int h = 0; h < C / 64; ++h) {
           // 64 columns per round trip: two 32-column TMEM loads, one wait
@@ -198,20 +199,36 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(pe0 + 8 * pb);
           }
+          // acc += P * scale.  With per-column B scales, two columns per
+          // packed fmul2 / ffma2 (each lane rounds like the scalar
+          // instruction): that path has a multiply per element on top of the
+          // FMA, and its promotion is issue-bound.
           if (B_TILE) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]),
-                                          __fmul_rn(sa, my_bs[h * 64 + j]), acc[h * 64 + j]);
-              acc[h * 64 + 32 + j] =
-                  __fmaf_rn(__uint_as_float(r1[j]), __fmul_rn(sa, my_bs[h * 64 + 32 + j]),
-                            acc[h * 64 + 32 + j]);
+            for (int j = 0; j < 64; j += 4) {
+              const float4 b4 = *reinterpret_cast<const float4 *>(&my_bs[h * 64 + j]);
+              const float2 s01 = __fmul2_rn(sa2, make_float2(b4.x, b4.y));
+              const float2 s23 = __fmul2_rn(sa2, make_float2(b4.z, b4.w));
+              const uint32_t *rr = j < 32 ? &r0[j] : &r1[j - 32];
+              acc2[h * 32 + j / 2] = __ffma2_rn(
+                  make_float2(__uint_as_float(rr[0]), __uint_as_float(rr[1])), s01,
+                  acc2[h * 32 + j / 2]);
+              acc2[h * 32 + j / 2 + 1] = __ffma2_rn(
+                  make_float2(__uint_as_float(rr[2]), __uint_as_float(rr[3])), s23,
+                  acc2[h * 32 + j / 2 + 1]);
             }
           } else {
+            // one scale for the whole row segment: scalar FFMAs (the packed
+            // form spills here and measured slower)
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              acc[h * 64 + j] = __fmaf_rn(__uint_as_float(r0[j]), sab, acc[h * 64 + j]);
-              acc[h * 64 + 32 + j] = __fmaf_rn(__uint_as_float(r1[j]), sab, acc[h * 64 + 32 + j]);
+            for (int j = 0; j < 16; ++j) {
+              acc2[h * 32 + j].x = __fmaf_rn(__uint_as_float(r0[2 * j]), sab, acc2[h * 32 + j].x);
+              acc2[h * 32 + j].y =
+                  __fmaf_rn(__uint_as_float(r0[2 * j + 1]), sab, acc2[h * 32 + j].y);
+              acc2[h * 32 + 16 + j].x =
+                  __fmaf_rn(__uint_as_float(r1[2 * j]), sab, acc2[h * 32 + 16 + j].x);
+              acc2[h * 32 + 16 + j].y =
+                  __fmaf_rn(__uint_as_float(r1[2 * j + 1]), sab, acc2[h * 32 + 16 + j].y);
             }
           }
         }
@@ -224,7 +241,10 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
           if (n0 < p.N) {
             float v[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = acc[c * 32 + j];
+            for (int j = 0; j < 16; ++j) {
+              v[2 * j] = acc2[c * 16 + j].x;
+              v[2 * j + 1] = acc2[c * 16 + j].y;
+            }
             run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
           }
         }

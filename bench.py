@@ -1087,6 +1087,35 @@ def main():
         stream=stream), QK, W, flush=flush)
     dual_bytes = n * 2 + 2 * n     # read x once, write q and q_t (scales are < 0.1%)
 
+    # ---- the same calls back to back on the stream, as a training step
+    # issues them: NROT distinct copies of the activation (each with its own
+    # outputs; 4 x 64 MiB, more than L2, so every call reads its input from
+    # DRAM), K rounds timed with one event pair, time per call.  A single
+    # call, as timed above, also pays the launch floor (an empty kernel
+    # measures about 3.6 us between two events); here that overlaps the
+    # previous kernel.
+    NROT = 4
+    xs = [xq] + [xq.clone() for _ in range(NROT - 1)]
+    rot = [{"q": torch.empty_like(qt), "s": torch.empty_like(st), "qt": torch.empty_like(qtt),
+            "st": torch.empty_like(stt), "a": torch.empty_like(am), "c": torch.empty_like(sc)}
+           for _ in range(NROT)]
+
+    def streamed(call):
+        def step():
+            for j in range(NROT):
+                call(xs[j], rot[j])
+        return time_steps(torch, dist, stream, step, QK, W) / NROT
+
+    sms_tile = streamed(lambda xj, o: fq.fp8_quantize_tile1x128(
+        xj, fq.E4M3, rows=True, q=o["q"], q_scales=o["s"], stream=stream))
+    sms_amax = streamed(lambda xj, o: fq.fp8_amax(xj, out=o["a"], stream=stream))
+    sms_tensor = streamed(lambda xj, o: fq.fp8_quantize_tensor_current(
+        xj, fq.E4M3, q=o["q"], amax=o["a"], scale=o["c"], stream=stream))
+    sms_tile2 = streamed(lambda xj, o: fq.fp8_quantize_tile1x128(
+        xj, fq.E4M3, rows=True, cols=True, q=o["q"], q_scales=o["s"], q_t=o["qt"],
+        qt_scales=o["st"], stream=stream))
+    del xs, rot
+
     # ---- accuracy on the same activation: MSE of the dequantised values on
     # the rows without outliers, 1x128 tiles against one scale per tensor
     # (analysis of the kernels' outputs, outside every timed region)
@@ -1201,6 +1230,21 @@ def main():
                           "bytes": tile_bytes, "frac": tile_gbps / hbm_peak},
             "amax": {"GB/s": gbps(2 * n, ms_amax), "us": ms_amax * 1e3,
                      "frac": gbps(2 * n, ms_amax) / hbm_peak},
+            "streamed": {
+                "note": ("per call, 4 distinct 64 MiB activations back to back on the "
+                         "stream (each read from DRAM), K rounds under one event pair; the "
+                         "single-call figures above also include the ~3.6 us launch floor "
+                         "between two events"),
+                "tile1x128": {"us": sms_tile * 1e3, "GB/s": gbps(tile_bytes, sms_tile),
+                              "frac": gbps(tile_bytes, sms_tile) / hbm_peak},
+                "amax": {"us": sms_amax * 1e3, "GB/s": gbps(2 * n, sms_amax),
+                         "frac": gbps(2 * n, sms_amax) / hbm_peak},
+                "tensor_current_over_3B": {"us": sms_tensor * 1e3,
+                                           "GB/s": gbps(3 * n, sms_tensor),
+                                           "frac": gbps(3 * n, sms_tensor) / hbm_peak},
+                "tile1x128_rows_and_cols": {"us": sms_tile2 * 1e3,
+                                            "GB/s": gbps(dual_bytes, sms_tile2),
+                                            "frac": gbps(dual_bytes, sms_tile2) / hbm_peak}},
             "tensor_current": {"GB/s (over 3 B/elem)": gbps(3 * n, ms_tensor),
                                "us": ms_tensor * 1e3,
                                "frac": gbps(3 * n, ms_tensor) / hbm_peak,

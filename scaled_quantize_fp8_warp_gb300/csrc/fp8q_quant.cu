@@ -34,6 +34,7 @@
 #include <cuda_fp8.h>
 
 #include <atomic>
+#include <mutex>
 #include <stdint.h>
 #include <string.h>
 
@@ -1006,16 +1007,56 @@ __global__ void __launch_bounds__(kQuantThreads, (QuantShape<InT, KM>::kMinBlock
 }
 
 // amax over a flat array: 16-byte loads, packed 16-bit max for bf16,
-// warp/CTA reduction, one atomicMax on the fp32 bit pattern per CTA (|x| bit
-// patterns order like the values; NaN patterns sort above Inf).
+// warp/CTA reduction; each CTA stores its maximum (as an fp32 bit pattern:
+// |x| bit patterns order like the values, NaN patterns above Inf) in its own
+// entry of a slot of g_amax_partials and takes a ticket, and the last CTA
+// reduces the partials with all its threads and writes the output.  The call
+// therefore needs no zeroing launch ahead of it, and no two CTAs contend on
+// one address except for the ticket.  Each launch takes its own slot
+// (round-robin), so launches that overlap in time do not share one.
+constexpr int kAmaxSlots = 32;
+constexpr int kAmaxMaxCtas = 8 * 256;   // partial entries per slot (grids of <= 8 CTAs per SM)
+__device__ unsigned int g_amax_partials[kAmaxSlots][kAmaxMaxCtas];
+__device__ unsigned int g_amax_tickets[kAmaxSlots];
+
+// Each CTA streams 32 KB chunks of x (chunk c = blockIdx.x + k gridDim.x)
+// through a ring of kAmaxStages shared-memory stages filled by bulk copies
+// (cp.async.bulk, completion counted on one mbarrier per stage); all 256
+// threads reduce each chunk from shared memory.  Bulk copies keep far more
+// bytes in flight per SM than per-thread 16-byte loads can.  The bytes after
+// the last whole chunk are read with plain loads.
+constexpr int kAmaxChunk = 32768;
+constexpr int kAmaxStages = 6;
+constexpr int kAmaxSmem = kAmaxStages * kAmaxChunk + 128;
+
 template <typename InT>
-__global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, int64_t n,
-                                                   unsigned int *out) {
-  constexpr int kVec = 16 / sizeof(InT);
-  const int64_t nvec = n / kVec;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+__global__ void __launch_bounds__(256, 1)
+    amax_kernel(const InT *__restrict__ x, int64_t n, unsigned int *out, int slot,
+                unsigned int *err) {
+  extern __shared__ uint8_t amax_smem[];
+  __shared__ __align__(8) uint64_t bars[kAmaxStages];
+  __shared__ uint32_t red[8];
+  __shared__ int last, abort_flag;
+  uint8_t *ring = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(amax_smem) + 127) & ~static_cast<uintptr_t>(127));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t nbytes = n * (int64_t)sizeof(InT);
+  const int64_t nchunks = nbytes / kAmaxChunk;
+  const int64_t mine = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint8_t *xb = reinterpret_cast<const uint8_t *>(x);
+  auto issue = [&](int64_t j) {   // thread 0: load this CTA's j-th chunk into stage j % S
+    const uint32_t bar = ptx::smem_u32(&bars[j % kAmaxStages]);
+    ptx::mbar_arrive_expect_tx(bar, kAmaxChunk);
+    ptx::bulk_load(ptx::smem_u32(ring + (j % kAmaxStages) * kAmaxChunk),
+                   xb + (blockIdx.x + j * gridDim.x) * (int64_t)kAmaxChunk, kAmaxChunk, bar);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kAmaxStages; ++s) ptx::mbar_init(ptx::smem_u32(&bars[s]), 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+    for (int64_t j = 0; j < mine && j < kAmaxStages; ++j) issue(j);
+  }
+  __syncthreads();
   uint32_t m = 0;
   auto upd = [&](uint4 w) {
     if (sizeof(InT) == 2) {
@@ -1030,33 +1071,46 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
       m = max(m, w.w & 0x7FFFFFFFu);
     }
   };
-#ifndef FP8Q_AMAX_UNROLL
-#define FP8Q_AMAX_UNROLL 8
-#endif
-  // FP8Q_AMAX_UNROLL 16-byte loads in flight per thread per round trip; the
-  // last round is predicated rather than finished one load at a time, so a
-  // thread never waits out more than one round trip per U loads
-  constexpr int U = FP8Q_AMAX_UNROLL;
-  for (; i + (U - 1) * stride < nvec; i += U * stride) {
-    uint4 w[U];
+  int64_t issued = mine < kAmaxStages ? mine : kAmaxStages;
+  for (int64_t j = 0; j < mine; ++j) {
+    const int s = (int)(j % kAmaxStages);
+    const bool ok = ptx::wait_bounded_warp(ptx::smem_u32(&bars[s]),
+                                           (uint32_t)((j / kAmaxStages) & 1), &abort_flag, err);
+    if (ok) {
+      const uint4 *st = reinterpret_cast<const uint4 *>(ring + s * kAmaxChunk);
 #pragma unroll
-    for (int u = 0; u < U; ++u) w[u] = __ldg(xv + i + u * stride);
-#pragma unroll
-    for (int u = 0; u < U; ++u) upd(w[u]);
+      for (int k = 0; k < kAmaxChunk / 16 / 256; ++k) upd(st[tid + k * 256]);
+    }
+    // every thread is done with stage s (or the CTA is aborting): refill it
+    if (__syncthreads_or(ok ? 0 : 1)) break;
+    if (tid == 0 && j + kAmaxStages < mine) {
+      issue(j + kAmaxStages);
+      issued = j + kAmaxStages + 1;
+    }
   }
-  if (i < nvec) {
-    uint4 w[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      w[u] = (i + u * stride < nvec) ? __ldg(xv + i + u * stride) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < U; ++u) upd(w[u]);
+  if (tid == 0 && abort_flag) {
+    // let the copies in flight land before the CTA exits (bounded)
+    for (int64_t j = issued > kAmaxStages ? issued - kAmaxStages : 0; j < issued; ++j) {
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(ptx::smem_u32(&bars[j % kAmaxStages]),
+                                 (uint32_t)((j / kAmaxStages) & 1)) &&
+             ptx::globaltimer_ns() - t0 < 200000000ull) {
+      }
+    }
   }
+  // the bytes after the last whole chunk, with plain loads
+  const int64_t tail0 = nchunks * kAmaxChunk;
+  const int64_t nvec_tail = (nbytes - tail0) / 16;
+  const uint4 *tv = reinterpret_cast<const uint4 *>(xb + tail0);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + tid; i < nvec_tail;
+       i += (int64_t)gridDim.x * blockDim.x)
+    upd(__ldg(tv + i));
   if (sizeof(InT) == 2) m = max(m & 0xFFFFu, m >> 16) << 16;
-  // scalar tail (fewer than kVec elements)
-  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (g < n - nvec * kVec) {
-    const int64_t k = nvec * kVec + g;
+  // the elements after the last whole 16 bytes
+  const int64_t first_scalar = (tail0 + nvec_tail * 16) / (int64_t)sizeof(InT);
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + tid;
+  if (g < n - first_scalar) {
+    const int64_t k = first_scalar + g;
     uint32_t b;
     if (sizeof(InT) == 2)
       b = ((uint32_t) reinterpret_cast<const uint16_t *>(x)[k] << 16) & 0x7FFFFFFFu;
@@ -1065,14 +1119,31 @@ __global__ void __launch_bounds__(256) amax_kernel(const InT *__restrict__ x, in
     m = max(m, b);
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
-  __shared__ uint32_t red[8];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) red[warp] = m;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  unsigned int *partials = g_amax_partials[slot];
+  if (tid == 0) {
     uint32_t r = red[0];
-    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = max(r, red[w]);
-    atomicMax(out, r);
+    for (int w = 1; w < 8; ++w) r = max(r, red[w]);
+    partials[blockIdx.x] = r;
+    __threadfence();                                   // the partial before the ticket
+    last = atomicAdd(&g_amax_tickets[slot], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  // the last CTA: every partial is visible (each was fenced before its ticket)
+  __threadfence();
+  uint32_t r = 0;
+  for (int k = tid; k < (int)gridDim.x; k += blockDim.x)
+    r = max(r, *reinterpret_cast<volatile unsigned int *>(&partials[k]));
+  r = __reduce_max_sync(0xFFFFFFFFu, r);
+  __syncthreads();
+  if (lane == 0) red[warp] = r;
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 0; w < 8; ++w) r = max(r, red[w]);
+    *out = r;
+    g_amax_tickets[slot] = 0u;
   }
 }
 
@@ -1184,19 +1255,38 @@ cudaError_t launch_quant2d(const QuantParams &p, cudaStream_t stream) {
 
 cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
                         cudaStream_t stream) {
-  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), stream);
-  if (e != cudaSuccess || n == 0) return e;
-  const int vec = in_dtype == FP8Q_DT_BF16 ? 8 : 4;
-  int64_t nvec = n / vec;
-  int64_t blocks = (nvec + 255) / 256;
-  const int64_t cap = (int64_t)sm_count() * 8;
+  // one CTA per SM (its ring takes 192 KB of shared memory), or one per
+  // whole chunk when there are fewer; n == 0 still runs one CTA, which
+  // writes 0
+  const int64_t nbytes = n * (in_dtype == FP8Q_DT_BF16 ? 2 : 4);
+  int64_t blocks = nbytes / kAmaxChunk;
+  int64_t cap = sm_count();
+  if (cap > kAmaxMaxCtas) cap = kAmaxMaxCtas;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  static std::atomic<unsigned int> next_slot{0};
+  const int slot = (int)(next_slot.fetch_add(1u) % kAmaxSlots);
   unsigned int *out = reinterpret_cast<unsigned int *>(amax);
+  unsigned int *err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidValue;
+  static bool attr_done[2] = {false, false};
+  const int t = in_dtype == FP8Q_DT_BF16 ? 0 : 1;
+  if (!attr_done[t]) {
+    cudaError_t e = t == 0 ? cudaFuncSetAttribute(amax_kernel<uint16_t>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  kAmaxSmem)
+                           : cudaFuncSetAttribute(amax_kernel<float>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  kAmaxSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[t] = true;
+  }
   if (in_dtype == FP8Q_DT_BF16)
-    amax_kernel<uint16_t><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint16_t *>(x), n, out);
+    amax_kernel<uint16_t><<<(unsigned)blocks, 256, kAmaxSmem, stream>>>(
+        static_cast<const uint16_t *>(x), n, out, slot, err);
   else
-    amax_kernel<float><<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const float *>(x), n, out);
+    amax_kernel<float><<<(unsigned)blocks, 256, kAmaxSmem, stream>>>(
+        static_cast<const float *>(x), n, out, slot, err);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,7 @@ PROFILE_CASES = {
     "quant_activation": ("the bench's 8192x4096 activation, 1x128 row tiles, E4M3, L2 flushed "
                          "before each of the three calls"),
     "quant_mx_dual": "16384x8192 bf16, MXFP8 1x32 row and 32x1 column blocks, E4M3",
+    "amax_activation": "the bench's 8192x4096 activation, amax, L2 flushed before each of three calls",
     "gemm_mx": "8192x8192x8192 MXFP8 x MXFP8 GEMM, bf16 out",
 }
 # One linear of the layer, its Fprop, Dgrad and Wgrad once each (three GEMM
@@ -152,13 +153,16 @@ def run_profile_case(case: str):
         out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         for _ in range(3):
             fq.fp8_gemm(A, B, out=out)
-    elif case == "quant_activation":
+    elif case in ("quant_activation", "amax_activation"):
         x, _ = workloads.quantize_activation()
         x = x.cuda()
         flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
         for _ in range(3):
             flush_buf.fill_(1.0)
-            fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True)
+            if case == "amax_activation":
+                fq.fp8_amax(x)
+            else:
+                fq.fp8_quantize_tile1x128(x, fq.E4M3, rows=True)
     else:
         x = workloads.normal((16384, 8192), 1.0, 902).cuda()
         for _ in range(3):

@@ -404,6 +404,70 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M,
                         void *y, int out_dtype, void *workspace,
                         size_t ws_bytes, cudaStream_t stream);
 
+/* ----------------------------------------- a linear layer's whole step */
+
+/* Bytes of workspace fp8_linear_train needs: the FP8 copies of x, w and
+ * grad_out in both orientations plus the recipe's scales (256-byte pieces);
+ * 0 for negative sizes, sizes whose element counts overflow, or a bad recipe. */
+size_t fp8q_linear_train_workspace_size(int recipe, int64_t M, int64_t N, int64_t K);
+
+/* The three GEMMs of one linear layer in training, each operand quantized
+ * on the fly ([fp8_parity] FP8Matmul: the forward quantizes x and w to E4M3
+ * and returns xq @ wq.T; the backward quantizes grad_out to E5M2 and returns
+ * gq @ wq and gq.T @ xq; [te_blog] "autocast mode": inputs are quantized
+ * dynamically before each GEMM):
+ *   y  [M, N] = x [M, K] . w [N, K]^T      (Fprop)
+ *   dx [M, K] = g [M, N] . w               (Dgrad)
+ *   dw [N, K] = g^T . x                    (Wgrad)
+ * with x, w and grad_out g (device, in_dtype) quantized under `recipe`, each
+ * into both orientations (the transposed copies feed Dgrad and Wgrad):
+ *   TENSOR_CURRENT: per-tensor scales from each tensor's own amax
+ *   TENSOR_DELAYED: per-tensor scales from hist_x / hist_w / hist_g (device
+ *                   state, required; each is updated as fp8_quantize_delayed
+ *                   does)
+ *   BLOCK:          1x128 tiles on x and g (row tiles for Fprop / Dgrad,
+ *                   column tiles for Wgrad), 128x128 blocks on w
+ *   MXFP8:          1x32 MXFP8 blocks on all three, in both orientations
+ * Outputs y, dx, dw are device out_dtype.  All work is enqueued on `stream`.
+ *   workspace: device, >= fp8q_linear_train_workspace_size, 256-byte aligned
+ * Alignment: M, N, K multiples of 16.
+ * Errors: INVALID_ARG, MISALIGNED, WORKSPACE, ARCH, CUDA. */
+int fp8_linear_train(const void *x, const void *w, const void *g, int in_dtype,
+                     int64_t M, int64_t N, int64_t K, int recipe,
+                     fp8q_amax_history *hist_x, fp8q_amax_history *hist_w,
+                     fp8q_amax_history *hist_g, void *y, void *dx, void *dw,
+                     int out_dtype, void *workspace, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/* Bytes of device workspace fp8_linear_train_host needs: that of
+ * fp8_linear_train plus device copies of x, w, g (in_dtype) and of y, dx, dw
+ * (out_dtype); 0 for invalid arguments. */
+size_t fp8q_linear_train_host_workspace_size(int recipe, int in_dtype, int out_dtype,
+                                             int64_t M, int64_t N, int64_t K);
+
+/* fp8_linear_train from and to HOST buffers: x_h, w_h, g_h and y_h, dx_h,
+ * dw_h are host memory (page-locked for the copies to overlap), copied in and
+ * out inside the call's work.  The copies run on two streams the library
+ * owns (one per direction, created on the first call on a device and kept
+ * until the process exits), ordered against `stream` by events:
+ *   - the copies in start after the work already queued on `stream`;
+ *   - x and w are quantized while g is still being copied in;
+ *   - y is copied out during the Dgrad, dx during the Wgrad;
+ *   - `stream` waits for the last copy out, so work queued on it after this
+ *     call sees the host outputs filled (synchronise `stream` before reading
+ *     them on the host).
+ * Calls from several host threads on one device are serialised internally
+ * while they enqueue.  The workspace must not be in use by other work.
+ *   workspace: device, >= fp8q_linear_train_host_workspace_size, 256-byte
+ *              aligned
+ * Arguments, alignment and errors otherwise as fp8_linear_train. */
+int fp8_linear_train_host(const void *x_h, const void *w_h, const void *g_h,
+                          int in_dtype, int64_t M, int64_t N, int64_t K,
+                          int recipe, fp8q_amax_history *hist_x,
+                          fp8q_amax_history *hist_w, fp8q_amax_history *hist_g,
+                          void *y_h, void *dx_h, void *dw_h, int out_dtype,
+                          void *workspace, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------ forward without a workspace */
 
 /* Size of the static scratch used by fp8_linear_autocast_noalloc. */

@@ -54,7 +54,8 @@ EXPORTS = (
     "fp8q_mx_scale_bytes", "fp8_quantize_block128x128", "fp8_gemm",
     "fp8_gemm_amax", "fp8_gemm_fprop",
     "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
-    "fp8_linear_autocast_noalloc",
+    "fp8_linear_autocast_noalloc", "fp8q_linear_train_workspace_size", "fp8_linear_train",
+    "fp8q_linear_train_host_workspace_size", "fp8_linear_train_host",
 )
 
 
@@ -113,6 +114,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                           P]),
             "fp8_linear_autocast_noalloc": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32,
                                                   P]),
+            "fp8q_linear_train_workspace_size": (SZ, [I32, I64, I64, I64]),
+            "fp8_linear_train": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P, I32,
+                                       P, SZ, P]),
+            "fp8q_linear_train_host_workspace_size": (SZ, [I32, I32, I32, I64, I64, I64]),
+            "fp8_linear_train_host": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P,
+                                            I32, P, SZ, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -154,6 +161,9 @@ def _in_dtype(x: torch.Tensor) -> int:
     if x.dtype == torch.float32:
         return DT_F32
     raise TypeError(f"input must be bfloat16 or float32, got {x.dtype}")
+
+
+_DT = {torch.bfloat16: DT_BF16, torch.float32: DT_F32}
 
 
 def _out_dtype(dt) -> int:
@@ -461,6 +471,58 @@ def fp8_linear_autocast(x, w, recipe=RECIPE_TENSOR_CURRENT, out_dtype=torch.bflo
         _ptr(out), _out_dtype(out.dtype), _ptr(workspace), workspace.numel(), _stream(stream)),
         "fp8_linear_autocast")
     return out
+
+
+def linear_train_workspace_size(recipe: int, M: int, N: int, K: int) -> int:
+    return int(lib().fp8q_linear_train_workspace_size(recipe, M, N, K))
+
+
+def fp8_linear_train(x, w, g, recipe=RECIPE_TENSOR_CURRENT, out_dtype=torch.bfloat16,
+                     hist_x: History | None = None, hist_w: History | None = None,
+                     hist_g: History | None = None, workspace=None, y=None, dx=None, dw=None,
+                     stream=None):
+    """One linear layer's Fprop, Dgrad and Wgrad with x, w, grad_out quantized
+    on the fly (device tensors).  Returns (y, dx, dw)."""
+    M, K = _rows_cols(x)
+    N = w.shape[0]
+    if workspace is None:
+        workspace = torch.empty(linear_train_workspace_size(recipe, M, N, K), dtype=torch.uint8,
+                                device=x.device)
+    y = y if y is not None else torch.empty((M, N), dtype=out_dtype, device=x.device)
+    dx = dx if dx is not None else torch.empty((M, K), dtype=out_dtype, device=x.device)
+    dw = dw if dw is not None else torch.empty((N, K), dtype=out_dtype, device=x.device)
+    hp = lambda h: _ptr(h.buf) if h else None
+    _check(lib().fp8_linear_train(
+        _ptr(x), _ptr(w), _ptr(g), _in_dtype(x), M, N, K, recipe, hp(hist_x), hp(hist_w),
+        hp(hist_g), _ptr(y), _ptr(dx), _ptr(dw), _out_dtype(y.dtype), _ptr(workspace),
+        workspace.numel(), _stream(stream)), "fp8_linear_train")
+    return y, dx, dw
+
+
+def linear_train_host_workspace_size(recipe: int, in_dtype, out_dtype, M: int, N: int,
+                                     K: int) -> int:
+    return int(lib().fp8q_linear_train_host_workspace_size(
+        recipe, _DT[in_dtype], _DT[out_dtype], M, N, K))
+
+
+def fp8_linear_train_host(x_h, w_h, g_h, y_h, dx_h, dw_h, workspace,
+                          recipe=RECIPE_TENSOR_CURRENT, hist_x: History | None = None,
+                          hist_w: History | None = None, hist_g: History | None = None,
+                          stream=None):
+    """fp8_linear_train from and to host tensors (pinned CPU tensors; the
+    copies happen inside the call's work on `stream`).  Outputs are filled
+    once `stream` has reached this call's end."""
+    M, K = x_h.shape
+    N = w_h.shape[0]
+    for t in (x_h, w_h, g_h, y_h, dx_h, dw_h):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors")
+    hp = lambda h: _ptr(h.buf) if h else None
+    _check(lib().fp8_linear_train_host(
+        x_h.data_ptr(), w_h.data_ptr(), g_h.data_ptr(), _DT[x_h.dtype], M, N, K, recipe,
+        hp(hist_x), hp(hist_w), hp(hist_g), y_h.data_ptr(), dx_h.data_ptr(), dw_h.data_ptr(),
+        _DT[y_h.dtype], _ptr(workspace), workspace.numel(), _stream(stream)),
+        "fp8_linear_train_host")
 
 
 #: size of the library's static scratch (FP8Q_NOALLOC_SCRATCH_BYTES)

@@ -673,3 +673,289 @@ int fp8_linear_autocast(const void *x, const void *w, int in_dtype, int64_t M, i
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------- a linear's whole step
+
+namespace {
+
+// Workspace carving of fp8_linear_train: FP8 copies of x, w, g in both
+// orientations, then the recipe's scales (256-byte aligned pieces).
+struct TrainLayout {
+  size_t qx, qxt, qw, qwt, qg, qgt;        // byte offsets of the FP8 copies
+  size_t sx, sxt, sw, swt, sg, sgt;        // scale arrays (or per-tensor scalars)
+  size_t ax, aw, ag;                       // per-tensor amax words
+  size_t total;
+};
+
+TrainLayout train_layout(int recipe, int64_t M, int64_t N, int64_t K) {
+  TrainLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += round256(bytes); return at; };
+  L.qx = take((size_t)(M * K));
+  L.qxt = take((size_t)(M * K));
+  L.qw = take((size_t)(N * K));
+  L.qwt = take((size_t)(N * K));
+  L.qg = take((size_t)(M * N));
+  L.qgt = take((size_t)(M * N));
+  const size_t f = sizeof(float);
+  if (recipe == FP8Q_RECIPE_BLOCK) {
+    L.sx = take(f * (size_t)(((K + 127) / 128) * M));          // x row tiles
+    L.sxt = take(f * (size_t)(((M + 127) / 128) * K));         // x column tiles
+    L.sw = take(f * (size_t)(((N + 127) / 128) * ((K + 127) / 128)));
+    L.sg = take(f * (size_t)(((N + 127) / 128) * M));          // g row tiles
+    L.sgt = take(f * (size_t)(((M + 127) / 128) * N));         // g column tiles
+  } else if (recipe == FP8Q_RECIPE_MXFP8) {
+    L.sx = take(fp8q_mx_scale_bytes(M, K));
+    L.sxt = take(fp8q_mx_scale_bytes(K, M));
+    L.sw = take(fp8q_mx_scale_bytes(N, K));
+    L.swt = take(fp8q_mx_scale_bytes(K, N));
+    L.sg = take(fp8q_mx_scale_bytes(M, N));
+    L.sgt = take(fp8q_mx_scale_bytes(N, M));
+  } else {
+    L.sx = take(f);
+    L.sw = take(f);
+    L.sg = take(f);
+    L.ax = take(f);
+    L.aw = take(f);
+    L.ag = take(f);
+  }
+  L.total = o;
+  return L;
+}
+
+bool valid_recipe(int r) {
+  return r == FP8Q_RECIPE_TENSOR_CURRENT || r == FP8Q_RECIPE_TENSOR_DELAYED ||
+         r == FP8Q_RECIPE_BLOCK || r == FP8Q_RECIPE_MXFP8;
+}
+
+int check_train_args(int in_dtype, int out_dtype, int64_t M, int64_t N, int64_t K, int recipe,
+                     fp8q_amax_history *hx, fp8q_amax_history *hw, fp8q_amax_history *hg) {
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype) || !valid_recipe(recipe))
+    return FP8Q_ERR_INVALID_ARG;
+  if (!linear_dims_ok(M, N, K) || M % 16 != 0 || N % 16 != 0 || K % 16 != 0)
+    return FP8Q_ERR_INVALID_ARG;
+  if (recipe == FP8Q_RECIPE_TENSOR_DELAYED && (hx == nullptr || hw == nullptr || hg == nullptr))
+    return FP8Q_ERR_INVALID_ARG;
+  return FP8Q_OK;
+}
+
+// Library-owned streams and events of fp8_linear_train_host, per device,
+// created on first use and kept until the process exits.  The mutex keeps
+// the record / wait sequences of concurrent host threads apart.
+struct HostStepRes {
+  std::once_flag once;
+  std::mutex mu;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t ev[8] = {};
+  bool ok = false;
+};
+HostStepRes g_host_step[kMaxDevices];
+
+HostStepRes *host_step_res() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostStepRes *r = &g_host_step[dev];
+  std::call_once(r->once, [r] {
+    bool ok = cudaStreamCreateWithFlags(&r->in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&r->out, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < 8; ++i)
+      ok = cudaEventCreateWithFlags(&r->ev[i], cudaEventDisableTiming) == cudaSuccess;
+    r->ok = ok;
+  });
+  return r->ok ? r : nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fp8q_linear_train_workspace_size(int recipe, int64_t M, int64_t N, int64_t K) {
+  if (!linear_dims_ok(M, N, K) || !valid_recipe(recipe)) return 0;
+  return train_layout(recipe, M, N, K).total;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The body of fp8_linear_train, with three optional events for the
+// host-buffer variant: the stream waits for g_ready before quantising g, and
+// records y_done after the Fprop and dx_done after the Dgrad.  Arguments are
+// validated by the callers.
+int train_impl(const void *x, const void *w, const void *g, int in_dtype, int64_t M, int64_t N,
+               int64_t K, int recipe, fp8q_amax_history *hist_x, fp8q_amax_history *hist_w,
+               fp8q_amax_history *hist_g, void *y, void *dx, void *dw, int out_dtype,
+               uint8_t *ws, cudaStream_t stream, cudaEvent_t g_ready, cudaEvent_t y_done,
+               cudaEvent_t dx_done) {
+  int rc;
+  const TrainLayout L = train_layout(recipe, M, N, K);
+  auto wait_g = [&]() {
+    return g_ready == nullptr || cudaStreamWaitEvent(stream, g_ready, 0) == cudaSuccess;
+  };
+  uint8_t *qx = ws + L.qx, *qxt = ws + L.qxt, *qw = ws + L.qw, *qwt = ws + L.qwt;
+  uint8_t *qg = ws + L.qg, *qgt = ws + L.qgt;
+  auto fp = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+  fp8q_operand fx{}, fw{}, dg{}, dwt{}, wgt{}, wxt{};   // fprop A/B, dgrad A/B, wgrad A/B
+  fx.data = qx;   fx.format = FP8Q_E4M3;
+  fw.data = qw;   fw.format = FP8Q_E4M3;
+  dg.data = qg;   dg.format = FP8Q_E5M2;
+  dwt.data = qwt; dwt.format = FP8Q_E4M3;
+  wgt.data = qgt; wgt.format = FP8Q_E5M2;
+  wxt.data = qxt; wxt.format = FP8Q_E4M3;
+  if (recipe == FP8Q_RECIPE_BLOCK) {
+    if ((rc = fp8_quantize_tile1x128(x, in_dtype, M, K, FP8Q_E4M3, qx, fp(L.sx), qxt, fp(L.sxt),
+                                     0, stream)) != FP8Q_OK ||
+        (rc = fp8_quantize_block128x128(w, in_dtype, N, K, FP8Q_E4M3, qw, qwt, fp(L.sw), 0,
+                                        stream)) != FP8Q_OK)
+      return rc;
+    if (!wait_g()) return FP8Q_ERR_CUDA;
+    if ((rc = fp8_quantize_tile1x128(g, in_dtype, M, N, FP8Q_E5M2, qg, fp(L.sg), qgt, fp(L.sgt),
+                                     0, stream)) != FP8Q_OK)
+      return rc;
+    const int64_t kbk = (K + 127) / 128;
+    fx.scaling = FP8Q_SCALE_TILE_1x128;   fx.scale = fp(L.sx);   fx.scale_stride_row = 1;
+    fx.scale_stride_k = M;
+    fw.scaling = FP8Q_SCALE_BLOCK_128x128; fw.scale = fp(L.sw); fw.scale_stride_row = kbk;
+    fw.scale_stride_k = 1;
+    dg.scaling = FP8Q_SCALE_TILE_1x128;   dg.scale = fp(L.sg);   dg.scale_stride_row = 1;
+    dg.scale_stride_k = M;
+    dwt.scaling = FP8Q_SCALE_BLOCK_128x128; dwt.scale = fp(L.sw); dwt.scale_stride_row = 1;
+    dwt.scale_stride_k = kbk;
+    wgt.scaling = FP8Q_SCALE_TILE_1x128;  wgt.scale = fp(L.sgt); wgt.scale_stride_row = 1;
+    wgt.scale_stride_k = N;
+    wxt.scaling = FP8Q_SCALE_TILE_1x128;  wxt.scale = fp(L.sxt); wxt.scale_stride_row = 1;
+    wxt.scale_stride_k = K;
+  } else if (recipe == FP8Q_RECIPE_MXFP8) {
+    if ((rc = fp8_quantize_mxfp8(x, in_dtype, M, K, FP8Q_E4M3, qx, ws + L.sx, qxt, ws + L.sxt,
+                                 stream)) != FP8Q_OK ||
+        (rc = fp8_quantize_mxfp8(w, in_dtype, N, K, FP8Q_E4M3, qw, ws + L.sw, qwt, ws + L.swt,
+                                 stream)) != FP8Q_OK)
+      return rc;
+    if (!wait_g()) return FP8Q_ERR_CUDA;
+    if ((rc = fp8_quantize_mxfp8(g, in_dtype, M, N, FP8Q_E5M2, qg, ws + L.sg, qgt, ws + L.sgt,
+                                 stream)) != FP8Q_OK)
+      return rc;
+    fp8q_operand *ops[6] = {&fx, &fw, &dg, &dwt, &wgt, &wxt};
+    const size_t offs[6] = {L.sx, L.sw, L.sg, L.swt, L.sgt, L.sxt};
+    for (int i = 0; i < 6; ++i) {
+      ops[i]->scaling = FP8Q_SCALE_MX_1x32;
+      ops[i]->mx_scale = ws + offs[i];
+    }
+  } else {
+    const bool delayed = recipe == FP8Q_RECIPE_TENSOR_DELAYED;
+    const void *src[3] = {x, w, g};
+    const int64_t rr[3] = {M, N, M}, cc[3] = {K, K, N};
+    const int fmt[3] = {FP8Q_E4M3, FP8Q_E4M3, FP8Q_E5M2};
+    uint8_t *q[3] = {qx, qw, qg}, *qt[3] = {qxt, qwt, qgt};
+    const size_t so[3] = {L.sx, L.sw, L.sg}, ao[3] = {L.ax, L.aw, L.ag};
+    fp8q_amax_history *h[3] = {hist_x, hist_w, hist_g};
+    for (int i = 0; i < 3; ++i) {
+      if (i == 2 && !wait_g()) return FP8Q_ERR_CUDA;
+      if (delayed)
+        rc = fp8_quantize_delayed(src[i], in_dtype, rr[i], cc[i], fmt[i], h[i], fp(so[i]), q[i],
+                                  qt[i], 0, stream);
+      else
+        rc = fp8_quantize_tensor_current(src[i], in_dtype, rr[i], cc[i], fmt[i], fp(ao[i]),
+                                         fp(so[i]), q[i], qt[i], 0, stream);
+      if (rc != FP8Q_OK) return rc;
+    }
+    fx.scaling = fw.scaling = dg.scaling = dwt.scaling = wgt.scaling = wxt.scaling =
+        FP8Q_SCALE_TENSOR;
+    fx.scale = wxt.scale = fp(L.sx);
+    fw.scale = dwt.scale = fp(L.sw);
+    dg.scale = wgt.scale = fp(L.sg);
+  }
+  if ((rc = fp8_gemm_fprop(&fx, &fw, y, out_dtype, M, N, K, stream)) != FP8Q_OK) return rc;
+  if (y_done != nullptr && cudaEventRecord(y_done, stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if ((rc = fp8_gemm_dgrad(&dg, &dwt, dx, out_dtype, M, N, K, stream)) != FP8Q_OK) return rc;
+  if (dx_done != nullptr && cudaEventRecord(dx_done, stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+  return fp8_gemm_wgrad(&wgt, &wxt, dw, out_dtype, M, N, K, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8_linear_train(const void *x, const void *w, const void *g, int in_dtype, int64_t M,
+                     int64_t N, int64_t K, int recipe, fp8q_amax_history *hist_x,
+                     fp8q_amax_history *hist_w, fp8q_amax_history *hist_g, void *y, void *dx,
+                     void *dw, int out_dtype, void *workspace, size_t ws_bytes,
+                     cudaStream_t stream) {
+  int rc = check_train_args(in_dtype, out_dtype, M, N, K, recipe, hist_x, hist_w, hist_g);
+  if (rc != FP8Q_OK) return rc;
+  if (workspace == nullptr || ws_bytes < train_layout(recipe, M, N, K).total)
+    return FP8Q_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FP8Q_ERR_MISALIGNED;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  return train_impl(x, w, g, in_dtype, M, N, K, recipe, hist_x, hist_w, hist_g, y, dx, dw,
+                    out_dtype, static_cast<uint8_t *>(workspace), stream, nullptr, nullptr,
+                    nullptr);
+}
+
+size_t fp8q_linear_train_host_workspace_size(int recipe, int in_dtype, int out_dtype, int64_t M,
+                                             int64_t N, int64_t K) {
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return 0;
+  const size_t base = fp8q_linear_train_workspace_size(recipe, M, N, K);
+  if (base == 0) return 0;
+  const size_t ib = in_dtype == FP8Q_DT_BF16 ? 2 : 4, ob = out_dtype == FP8Q_DT_BF16 ? 2 : 4;
+  return base + round256(ib * (size_t)(M * K)) + round256(ib * (size_t)(N * K)) +
+         round256(ib * (size_t)(M * N)) + round256(ob * (size_t)(M * N)) +
+         round256(ob * (size_t)(M * K)) + round256(ob * (size_t)(N * K));
+}
+
+int fp8_linear_train_host(const void *x_h, const void *w_h, const void *g_h, int in_dtype,
+                          int64_t M, int64_t N, int64_t K, int recipe,
+                          fp8q_amax_history *hist_x, fp8q_amax_history *hist_w,
+                          fp8q_amax_history *hist_g, void *y_h, void *dx_h, void *dw_h,
+                          int out_dtype, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_train_args(in_dtype, out_dtype, M, N, K, recipe, hist_x, hist_w, hist_g);
+  if (rc != FP8Q_OK) return rc;
+  const size_t need = fp8q_linear_train_host_workspace_size(recipe, in_dtype, out_dtype, M, N, K);
+  if (workspace == nullptr || ws_bytes < need) return FP8Q_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return FP8Q_ERR_MISALIGNED;
+  const bool any = M > 0 && N > 0 && K > 0;
+  if (any && (x_h == nullptr || w_h == nullptr || g_h == nullptr || y_h == nullptr ||
+              dx_h == nullptr || dw_h == nullptr))
+    return FP8Q_ERR_INVALID_ARG;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  HostStepRes *r = host_step_res();
+  if (r == nullptr) return FP8Q_ERR_CUDA;
+  const size_t ib = in_dtype == FP8Q_DT_BF16 ? 2 : 4, ob = out_dtype == FP8Q_DT_BF16 ? 2 : 4;
+  const size_t bx = ib * (size_t)(M * K), bw = ib * (size_t)(N * K), bg = ib * (size_t)(M * N);
+  const size_t by = ob * (size_t)(M * N), bdx = ob * (size_t)(M * K), bdw = ob * (size_t)(N * K);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  const size_t base = fp8q_linear_train_workspace_size(recipe, M, N, K);
+  uint8_t *dxin = ws + base, *dwin = dxin + round256(bx), *dgin = dwin + round256(bw);
+  uint8_t *dy = dgin + round256(bg), *ddx = dy + round256(by), *ddw = ddx + round256(bdx);
+  std::lock_guard<std::mutex> lock(r->mu);
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  cudaEvent_t *ev = r->ev;
+  // copies in: after everything already on the caller's stream (the
+  // workspace may still be in use there); x and w first, g after
+  if (!ok(cudaEventRecord(ev[0], stream)) || !ok(cudaStreamWaitEvent(r->in, ev[0], 0)) ||
+      !ok(cudaMemcpyAsync(dxin, x_h, bx, cudaMemcpyHostToDevice, r->in)) ||
+      !ok(cudaMemcpyAsync(dwin, w_h, bw, cudaMemcpyHostToDevice, r->in)) ||
+      !ok(cudaEventRecord(ev[1], r->in)) ||
+      !ok(cudaMemcpyAsync(dgin, g_h, bg, cudaMemcpyHostToDevice, r->in)) ||
+      !ok(cudaEventRecord(ev[2], r->in)) || !ok(cudaStreamWaitEvent(stream, ev[1], 0)))
+    return FP8Q_ERR_CUDA;
+  // the step on the caller's stream: x and w are quantised while g is still
+  // being copied in (the stream waits for it only before quantising g)
+  if ((rc = train_impl(dxin, dwin, dgin, in_dtype, M, N, K, recipe, hist_x, hist_w, hist_g, dy,
+                       ddx, ddw, out_dtype, ws, stream, ev[2], ev[3], ev[4])) != FP8Q_OK)
+    return rc;
+  // copies out on the library's out stream as each output is done (y during
+  // the Dgrad, dx during the Wgrad), then the caller's stream waits for the
+  // last, so work queued after this call sees the host buffers filled
+  if (!ok(cudaStreamWaitEvent(r->out, ev[3], 0)) ||
+      !ok(cudaMemcpyAsync(y_h, dy, by, cudaMemcpyDeviceToHost, r->out)) ||
+      !ok(cudaStreamWaitEvent(r->out, ev[4], 0)) ||
+      !ok(cudaMemcpyAsync(dx_h, ddx, bdx, cudaMemcpyDeviceToHost, r->out)) ||
+      !ok(cudaEventRecord(ev[5], stream)) || !ok(cudaStreamWaitEvent(r->out, ev[5], 0)) ||
+      !ok(cudaMemcpyAsync(dw_h, ddw, bdw, cudaMemcpyDeviceToHost, r->out)) ||
+      !ok(cudaEventRecord(ev[6], r->out)) || !ok(cudaStreamWaitEvent(stream, ev[6], 0)))
+    return FP8Q_ERR_CUDA;
+  return FP8Q_OK;
+}
+
+}  // extern "C"

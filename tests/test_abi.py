@@ -222,6 +222,31 @@ def test_linear_sizes_that_overflow_are_rejected(lib):
     assert lib.fp8q_linear_workspace_size(fq.RECIPE_TENSOR_CURRENT, 1 << 20, 16, 1 << 20) > 0
 
 
+def test_linear_train_validation_before_device(lib):
+    """fp8_linear_train(_host): M, N, K multiples of 16, a valid recipe, the
+    three histories for delayed scaling, a large enough 256-byte aligned
+    workspace -- all checked before any device work."""
+    import scaled_quantize_fp8_warp_gb300 as fq
+    P = ctypes.c_void_p
+    a = P(0x10000)
+    need = lib.fp8q_linear_train_workspace_size(fq.RECIPE_BLOCK, 256, 128, 64)
+    assert need > 0
+    assert lib.fp8q_linear_train_workspace_size(9, 256, 128, 64) == 0
+    assert lib.fp8q_linear_train_workspace_size(fq.RECIPE_BLOCK, -1, 128, 64) == 0
+    hneed = lib.fp8q_linear_train_host_workspace_size(fq.RECIPE_BLOCK, fq.DT_BF16, fq.DT_BF16,
+                                                      256, 128, 64)
+    assert hneed == need + 2 * (256 * 64 + 128 * 64 + 256 * 128) * 2
+    args = lambda M, N, K, rec, ws, wsz: (a, a, a, fq.DT_BF16, M, N, K, rec, None, None, None,
+                                          a, a, a, fq.DT_BF16, ws, wsz, None)
+    for fn in (lib.fp8_linear_train, lib.fp8_linear_train_host):
+        assert fn(*args(256, 128, 72, fq.RECIPE_BLOCK, a, 1 << 30)) == 1       # K % 16
+        assert fn(*args(200, 128, 64, fq.RECIPE_BLOCK, a, 1 << 30)) == 1       # M % 16
+        assert fn(*args(256, 128, 64, 7, a, 1 << 30)) == 1                     # recipe
+        assert fn(*args(256, 128, 64, fq.RECIPE_TENSOR_DELAYED, a, 1 << 30)) == 1   # histories
+        assert fn(*args(256, 128, 64, fq.RECIPE_BLOCK, a, 64)) == 4            # workspace
+        assert fn(*args(256, 128, 64, fq.RECIPE_BLOCK, P(0x10010), 1 << 30)) == 2   # alignment
+
+
 def test_workspace_size_formula(lib):
     import scaled_quantize_fp8_warp_gb300 as fq
     M, N, K = 15872, 4096, 4096

@@ -397,6 +397,8 @@ class LayerState:
                 L["dx_h"] = torch.empty((M, K), dtype=bf16).pin_memory()
                 L["dw_h"] = torch.empty((N, K), dtype=bf16).pin_memory()
                 self.d2h_bytes += 2 * (M * N + M * K + N * K)
+                L["ws_h"] = e((fq.linear_train_host_workspace_size(
+                    fq.RECIPE_TENSOR_CURRENT, bf16, bf16, M, N, K),), u8)
             self.linears.append(L)
         self.hist_g = []
         for i, L in enumerate(self.linears):
@@ -473,6 +475,7 @@ class Runner:
         self.mops = state.mx_operands()
         self.gemm_events = None   # list of (start, end, flops, (linear, role)) when recording
         self._cin, self._cout = self.torch.cuda.Stream(), self.torch.cuda.Stream()
+        self._lin_streams = [self.torch.cuda.Stream() for _ in state.linears]
 
     def _gemm(self, role, A, B, C, linear=0):
         fq, torch = self.fq, self.torch
@@ -596,47 +599,25 @@ class Runner:
         self.gemms(self.rops)
 
     # end to end: host inputs in, host outputs out --------------------------
-    def e2e_tensor(self):
-        """One step with the inputs copied in from pinned host memory and the
-        three outputs of every linear layer copied back, pipelined over three
-        streams at the granularity of single tensors: each tensor's amax and
-        cast wait only for that tensor's copy-in, and each output's copy-out
-        waits only for the GEMM that wrote it, so transfers in both directions
-        overlap the layer's work (everything is ordered after the step's start
-        on the compute stream, and the compute stream waits for the last
-        copy-out)."""
+    def e2e_host(self):
+        """One step through the C-ABI's host-buffer entry point: for each
+        linear one fp8_linear_train_host call (per-tensor current scaling)
+        from its pinned x, w and grad_out to its pinned y, dx and dw.  The
+        library copies in and out on its own two streams; each call is issued
+        on a stream of its own (all forked from the step's start on the
+        compute stream and joined at its end), with a workspace of its own,
+        so a linear's copies in queue right behind the previous linear's
+        instead of waiting for its GEMMs."""
         torch, fq, st = self.torch, self.fq, self.stream
         start = torch.cuda.Event()
         start.record(st)
-        self._cin.wait_event(start)
-        self._cout.wait_event(start)
-        arrived = []
-        with torch.cuda.stream(self._cin):
-            for L in self.s.linears:
-                evs = {}
-                for k in "xwg":
-                    L[k].copy_(L[k + "_h"], non_blocking=True)
-                    evs[k] = torch.cuda.Event()
-                    evs[k].record(self._cin)
-                arrived.append(evs)
-        for i, (L, o) in enumerate(zip(self.s.linears, self.tops)):
-            ev = arrived[i]
-            for k, fmt in (("x", fq.E4M3), ("w", fq.E4M3), ("g", fq.E5M2)):
-                st.wait_event(ev[k])
-                fq.fp8_amax(L[k], out=L["a" + k], stream=st)
-                fq.fp8_quantize_tensor(L[k], fmt, L["a" + k], want_q=True, want_qt=True,
-                                       q=L["q" + k], q_t=L["q" + k + "t"], scale=L["t" + k],
-                                       stream=st)
-            for role, out in (("fprop", "y"), ("dgrad", "dx"), ("wgrad", "dw")):
-                self._gemm(role, *o[role], i)
-                done = torch.cuda.Event()
-                done.record(st)
-                self._cout.wait_event(done)
-                with torch.cuda.stream(self._cout):
-                    L[out + "_h"].copy_(L[out], non_blocking=True)
-        fin = torch.cuda.Event()
-        fin.record(self._cout)
-        st.wait_event(fin)
+        for L, s in zip(self.s.linears, self._lin_streams):
+            s.wait_event(start)
+            fq.fp8_linear_train_host(L["x_h"], L["w_h"], L["g_h"], L["y_h"], L["dx_h"],
+                                     L["dw_h"], L["ws_h"], recipe=fq.RECIPE_TENSOR_CURRENT,
+                                     stream=s)
+        for s in self._lin_streams:
+            st.wait_stream(s)
 
     def link_rates(self, reps: int = 3):
         """Host<->device copy rates over this step's own pinned buffers: the
@@ -668,20 +649,6 @@ class Runner:
         hb, db = self.s.h2d_bytes, self.s.d2h_bytes
         return {"h2d_gbs": hb / t_in / 1e9, "d2h_gbs": db / t_out / 1e9,
                 "both_gbs": (hb + db) / t_both / 1e9, "floor_ms": t_both * 1e3}
-
-    def e2e_tensor_serial(self):
-        st = self.stream
-        with self.torch.cuda.stream(st):
-            for L in self.s.linears:
-                L["x"].copy_(L["x_h"], non_blocking=True)
-                L["w"].copy_(L["w_h"], non_blocking=True)
-                L["g"].copy_(L["g_h"], non_blocking=True)
-        self.tensor_autocast(False)
-        with self.torch.cuda.stream(st):
-            for L in self.s.linears:
-                L["y_h"].copy_(L["y"], non_blocking=True)
-                L["dx_h"].copy_(L["dx"], non_blocking=True)
-                L["dw_h"].copy_(L["dw"], non_blocking=True)
 
 
 def time_steps(torch, dist, stream, fn, steps, warmup, flush=None, record=None, clk=None):
@@ -955,7 +922,7 @@ def main():
     # are allocated: when the first host<->device round trip came only after
     # the device-resident phases, the timed step ran 29-40 ms instead of
     # ~20 ms, on the same box and build.
-    run.e2e_tensor()
+    run.e2e_host()
     torch.cuda.synchronize()
     flops = state.flops
 
@@ -1037,7 +1004,7 @@ def main():
     # ---- end to end through host buffers (headline recipe), with the host
     # link's own rates over the same buffers just before, since they bound it
     link = run.link_rates()
-    ms_e2e = time_steps(torch, dist, stream, run.e2e_tensor, max(2, K // 2), W)
+    ms_e2e = time_steps(torch, dist, stream, run.e2e_host, max(2, K // 2), W)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
     xq, out_rows = workloads.quantize_activation()
@@ -1290,7 +1257,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": tf(ms_e2e), "unit": "TFLOP/s",
                 "ms_per_step": ms_e2e, "h2d_bytes_per_step": state.h2d_bytes,
-                "d2h_bytes_per_step": state.d2h_bytes, "host_link": link},
+                "d2h_bytes_per_step": state.d2h_bytes, "host_link": link,
+                "how": ("4 fp8_linear_train_host C-ABI calls per step (per-tensor current "
+                        "scaling), pinned host x, w, grad_out in and y, dx, dw out")},
         "gpu_launches": Runner.tensor_autocast.launches * K,
         "clocks": clk.summary(),
     }

@@ -10,14 +10,17 @@ namespace gemm {
 namespace {
 
 // ------------------------------------------------------------------------
-// Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0) and the MMA
-// issuer (warp 1); NWG promotion warpgroups follow, warpgroup g owning tile
-// columns [g C, g C + C) with C = BN / NWG.  A carries 1x128 tile scales; B
-// carries 128x128 block scales (B_TILE = false) or 1x128 tile scales
-// (B_TILE = true).  Each 128-wide K block is accumulated into one of two
-// TMEM buffers of BN columns; the promotion warps load their C columns of it
-// (64 per round trip), hand the buffer back, and add it into fp32 registers
-// with the block's scale product.
+// Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0), the MMA
+// issuer (warp 1) and the scale warp (warp 2); NWG promotion warpgroups
+// follow, warpgroup g owning tile columns [g C, g C + C) with C = BN / NWG.
+// A carries 1x128 tile scales; B carries 128x128 block scales (B_TILE =
+// false) or 1x128 tile scales (B_TILE = true).  Each 128-wide K block is
+// accumulated into one of two TMEM buffers of BN columns; the promotion warps
+// load their C columns of it (64 per round trip), hand the buffer back, and
+// add it into fp32 registers with the block's scale product.  The scales
+// reach them through a shared-memory ring that the scale warp fills with
+// cp.async up to kScaleSlots K blocks ahead, so no global-load latency sits
+// in the promotion loop.
 //
 // Register split (setmaxnreg inside each role's branch): the launch of
 // 128 (1 + NWG) threads gets kLaunchRegs per thread; warpgroup 0 drops to
@@ -30,6 +33,7 @@ struct BSConfig {
   static constexpr int kThreads = 128 * (1 + NWG);
   static constexpr int kCols = BN / NWG;                 // columns per promotion warpgroup
   static constexpr int kStages = BN <= 192 ? 5 : 4;
+  static constexpr int kScaleSlots = 8;                  // K blocks of scales staged ahead
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
   static constexpr int kLowRegs = NWG == 2 ? 40 : 56;
   static constexpr int kHighRegs = ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8 > 232
@@ -48,11 +52,17 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
                             const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
   using Cfg = BSConfig<BN, NWG>;
   constexpr int STAGES = Cfg::kStages;
+  constexpr int SS = Cfg::kScaleSlots;
   constexpr int C = Cfg::kCols;
   constexpr int NPW = 4 * NWG;   // promotion warps
   using L = Layout<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(16) float sh_bscale[NPW][C];  // per promotion warp: B tile scales
+  // Scale ring: per K block, the tile's 128 A scales and its B scales (BN
+  // column scales, or one 128x128 block scale per promotion warpgroup),
+  // copied in ahead of use by the scale warp.
+  __shared__ __align__(16) float sh_sa[SS][kBM];
+  __shared__ __align__(16) float sh_sb[SS][B_TILE ? BN : 4];
+  __shared__ __align__(8) uint64_t sh_sbar[2 * SS];   // full, empty
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;
@@ -60,6 +70,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
   const uint32_t pf0 = bars + 8 * (2 * STAGES), pe0 = pf0 + 16;
   const uint32_t drain = pe0 + 16;
+  const uint32_t sfull0 = smem_u32(&sh_sbar[0]), sempty0 = sfull0 + 8 * SS;
   const uint32_t slot = bars + L::kBarBytes;
   uint8_t *slot_ptr = smem_raw + (slot - raw);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(slot_ptr + 4);
@@ -73,6 +84,10 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(pf0 + 8 * b, 1);
       mbar_init(pe0 + 8 * b, NPW);
+    }
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(sfull0 + 8 * s, 32);      // one cp.async arrival per lane of the scale warp
+      mbar_init(sempty0 + 8 * s, NPW);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -119,72 +134,83 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
         drain_mma(drain, abort_flag);
       }
       __syncwarp();
+    } else if (warp == 2) {
+      // Scale warp: every lane copies its share of each K block's scales into
+      // the next ring slot with cp.async (rows / columns past the matrix are
+      // zero-filled without a read) and arrives once its copies have landed;
+      // the promotion warps release the slot after their FMAs.
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int mt, nt;
+        tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt, kBlockGroupM, 0);
+        const int64_t m0 = (int64_t)mt * kBM, n0 = (int64_t)nt * BN;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t ss = it % SS, sph = (it / SS) & 1u;
+          if (!wait_bounded_warp(sempty0 + 8 * ss, sph ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t da = smem_u32(&sh_sa[ss][0]), db = smem_u32(&sh_sb[ss][0]);
+#pragma unroll
+          for (int u = 0; u < kBM / 32; ++u) {
+            const int r = lane + 32 * u;
+            const bool v = m0 + r < p.M;
+            const float *src = v ? p.scale_a + (kb * p.a_stride_k + (m0 + r) * p.a_stride_row)
+                                 : p.scale_a;
+            cp_async_4(da + 4 * r, src, v ? 4u : 0u);
+          }
+          if (B_TILE) {
+#pragma unroll
+            for (int u = 0; u < BN / 32; ++u) {
+              const int c = lane + 32 * u;
+              const bool v = n0 + c < p.N;
+              const float *src = v ? p.scale_b + (kb * p.b_stride_k + (n0 + c) * p.b_stride_row)
+                                   : p.scale_b;
+              cp_async_4(db + 4 * c, src, v ? 4u : 0u);
+            }
+          } else if (lane < NWG) {
+            // warpgroup `lane` covers columns [n0 + lane C, n0 + (lane + 1) C),
+            // all inside one 128-column block
+            const int64_t nc = n0 + lane * C;
+            const bool v = nc < p.N;
+            const float *src = v ? p.scale_b + ((nc / 128) * p.b_stride_row + kb * p.b_stride_k)
+                                 : p.scale_b;
+            cp_async_4(db + 4 * lane, src, v ? 4u : 0u);
+          }
+          cp_async_mbar_arrive(sfull0 + 8 * ss);
+        }
+      }
+      cp_async_wait_all();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kHighRegs));
     const int pw = warp - 4;              // promotion warp 0 .. NPW-1
     const int wg = pw >> 2;
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
-    float *my_bs = sh_bscale[pw];
-    constexpr int kPerLane = C / 32;      // B tile scales each lane stages (2 or 4)
     uint32_t it = 0, run_max = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt, kBlockGroupM, 0);
       const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
-      const bool m_ok = m < p.M;
       const int64_t ncol0 = (int64_t)nt * BN + wg * C;   // first column of this warpgroup
-      const int64_t nl = ncol0 + lane * kPerLane;         // this lane's B-scale columns
-      auto load_sa = [&](int kb) -> float {
-        return m_ok ? p.scale_a[kb * p.a_stride_k + m * p.a_stride_row] : 0.0f;
-      };
-      // Block scales: a warpgroup's C columns may straddle two 128-column
-      // blocks when C = 64 only if ncol0 % 128 == 64; both halves of a
-      // 64-column group lie in one block, so one scale serves the group.
-      auto load_sb = [&](int kb) -> float {
-        return ncol0 < p.N ? p.scale_b[(ncol0 / 128) * p.b_stride_row + kb * p.b_stride_k] : 0.0f;
-      };
       float2 acc2[C / 2];   // columns (2 j, 2 j + 1)
 #pragma unroll
       for (int j = 0; j < C / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
-      float sa_next = load_sa(0);
-      float sb_next = B_TILE ? 0.0f : load_sb(0);
-      float sbt_next[kPerLane];
-      if (B_TILE) {
-#pragma unroll
-        for (int u = 0; u < kPerLane; ++u)
-          sbt_next[u] = (nl + u < p.N) ? p.scale_b[(nl + u) * p.b_stride_row] : 0.0f;
-      }
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const float sa = sa_next;
-        const float sb = sb_next;
-        if (B_TILE) {
-          __syncwarp();
-#pragma unroll
-          for (int u = 0; u < kPerLane; ++u) my_bs[lane * kPerLane + u] = sbt_next[u];
-          __syncwarp();
-        }
-        if (kb + 1 < nkb) {
-          sa_next = load_sa(kb + 1);
-          if (B_TILE) {
-#pragma unroll
-            for (int u = 0; u < kPerLane; ++u)
-              sbt_next[u] = (nl + u < p.N)
-                                ? p.scale_b[(kb + 1) * p.b_stride_k + (nl + u) * p.b_stride_row]
-                                : 0.0f;
-          } else {
-            sb_next = load_sb(kb + 1);
-          }
-        }
+        const uint32_t ss = it % SS, sph = (it / SS) & 1u;
         const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-        if (!wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
+        if (!wait_bounded_warp(sfull0 + 8 * ss, sph, abort_flag, p.err) ||
+            !wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float sab = __fmul_rn(sa, sb);
+        const float sa = sh_sa[ss][quarter * 32 + lane];
+        const float sab = B_TILE ? 0.0f : __fmul_rn(sa, sh_sb[ss][wg]);
         const float2 sa2 = make_float2(sa, sa);
+        const float *bs = &sh_sb[ss][B_TILE ? wg * C : 0];
 #pragma unroll
         for (int h = 0; h < C / 64; ++h) {
           // 64 columns per round trip: two 32-column TMEM loads, one wait
@@ -206,7 +232,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
           if (B_TILE) {
 #pragma unroll
             for (int j = 0; j < 64; j += 4) {
-              const float4 b4 = *reinterpret_cast<const float4 *>(&my_bs[h * 64 + j]);
+              const float4 b4 = *reinterpret_cast<const float4 *>(&bs[h * 64 + j]);
               const float2 s01 = __fmul2_rn(sa2, make_float2(b4.x, b4.y));
               const float2 s23 = __fmul2_rn(sa2, make_float2(b4.z, b4.w));
               const uint32_t *rr = j < 32 ? &r0[j] : &r1[j - 32];
@@ -232,9 +258,12 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
             }
           }
         }
+        // this K block's scales have been read: hand the slot back
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
       }
       if (!ok) break;
-      if (m_ok) {
+      if (m < p.M) {
 #pragma unroll
         for (int c = 0; c < C / 32; ++c) {
           const int64_t n0 = ncol0 + c * 32;

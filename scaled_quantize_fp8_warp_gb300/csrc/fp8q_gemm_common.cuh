@@ -21,18 +21,14 @@ using namespace ptx;
 constexpr int kBM = 128;
 constexpr int kBK = 128;            // bytes = FP8 elements per K block
 constexpr int kUmmaK = 32;          // K per tcgen05.mma for 8-bit inputs
-// Tile width and promotion warpgroups of the tile/block-scaled kernel.
-#ifndef FP8Q_BLOCK_BN
-#define FP8Q_BLOCK_BN 256
-#define FP8Q_BLOCK_WG 2
-#endif
 // Per-tensor / row scaling at N > 128 runs on CTA pairs (cta_group::2) with
 // kPairAcc TMEM accumulators of 256 columns each and a ring of kPairStages
 // 32 KB stages per CTA.
 constexpr int kPairAcc = 2;
 constexpr int kPairStages = 6;
-constexpr int kBlockScaledBN = FP8Q_BLOCK_BN;
-constexpr int kBlockScaledWG = FP8Q_BLOCK_WG;
+// Tile width and promotion warpgroups of the tile/block-scaled kernel.
+constexpr int kBlockScaledBN = 256;
+constexpr int kBlockScaledWG = 2;
 constexpr int kMxBN = 256;   // N per tile of the MXFP8 kernel
 // Raster of the block-scaled kernel: groups of 16 M tiles, M fastest.  Its
 // promotion warps use the constant (no registers to spare for a runtime

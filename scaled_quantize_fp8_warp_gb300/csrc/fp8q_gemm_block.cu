@@ -19,8 +19,10 @@ namespace {
 // load their C columns of it (64 per round trip), hand the buffer back, and
 // add it into fp32 registers with the block's scale product.  The scales
 // reach them through a shared-memory ring that the scale warp fills with
-// cp.async up to kScaleSlots K blocks ahead, so no global-load latency sits
-// in the promotion loop.
+// cp.async, kScaleGroup K blocks per slot and kScaleSlots slots ahead, so no
+// global-load latency sits in the promotion loop and its slot handshake
+// (two shared-memory barrier operations, each a few hundred cycles while the
+// MMAs stream operands through shared memory) is paid once per group.
 //
 // Register split (setmaxnreg inside each role's branch): the launch of
 // 128 (1 + NWG) threads gets kLaunchRegs per thread; warpgroup 0 drops to
@@ -33,7 +35,8 @@ struct BSConfig {
   static constexpr int kThreads = 128 * (1 + NWG);
   static constexpr int kCols = BN / NWG;                 // columns per promotion warpgroup
   static constexpr int kStages = BN <= 192 ? 5 : 4;
-  static constexpr int kScaleSlots = 8;                  // K blocks of scales staged ahead
+  static constexpr int kScaleGroup = 4;                  // K blocks of scales per ring slot
+  static constexpr int kScaleSlots = 4;                  // ring slots
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
   static constexpr int kLowRegs = NWG == 2 ? 40 : 56;
   static constexpr int kHighRegs = ((65536 - 128 * kLowRegs) / (128 * NWG)) / 8 * 8 > 232
@@ -53,6 +56,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
   using Cfg = BSConfig<BN, NWG>;
   constexpr int STAGES = Cfg::kStages;
   constexpr int SS = Cfg::kScaleSlots;
+  constexpr int KG = Cfg::kScaleGroup;
   constexpr int C = Cfg::kCols;
   constexpr int NPW = 4 * NWG;   // promotion warps
   using L = Layout<BN, STAGES>;
@@ -60,8 +64,8 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
   // Scale ring: per K block, the tile's 128 A scales and its B scales (BN
   // column scales, or one 128x128 block scale per promotion warpgroup),
   // copied in ahead of use by the scale warp.
-  __shared__ __align__(16) float sh_sa[SS][kBM];
-  __shared__ __align__(16) float sh_sb[SS][B_TILE ? BN : 4];
+  __shared__ __align__(16) float sh_sa[SS][KG][kBM];
+  __shared__ __align__(16) float sh_sb[SS][KG][B_TILE ? BN : 4];
   __shared__ __align__(8) uint64_t sh_sbar[2 * SS];   // full, empty
 
   const uint32_t raw = smem_u32(smem_raw);
@@ -136,9 +140,11 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
       __syncwarp();
     } else if (warp == 2) {
       // Scale warp: every lane copies its share of each K block's scales into
-      // the next ring slot with cp.async (rows / columns past the matrix are
-      // zero-filled without a read) and arrives once its copies have landed;
-      // the promotion warps release the slot after their FMAs.
+      // the ring with cp.async (rows / columns past the matrix are
+      // zero-filled without a read), KG consecutive K blocks of the CTA's
+      // sequence per slot, and arrives once its copies for the slot have
+      // landed (or when its sequence ends inside a slot); the promotion warps
+      // release a slot after the FMAs of its last K block.
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -146,12 +152,12 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
         tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt, kBlockGroupM, 0);
         const int64_t m0 = (int64_t)mt * kBM, n0 = (int64_t)nt * BN;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const uint32_t ss = it % SS, sph = (it / SS) & 1u;
-          if (!wait_bounded_warp(sempty0 + 8 * ss, sph ^ 1u, abort_flag, p.err)) {
+          const uint32_t grp = it / KG, ss = grp % SS, sph = (grp / SS) & 1u, j = it % KG;
+          if (j == 0 && !wait_bounded_warp(sempty0 + 8 * ss, sph ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t da = smem_u32(&sh_sa[ss][0]), db = smem_u32(&sh_sb[ss][0]);
+          const uint32_t da = smem_u32(&sh_sa[ss][j][0]), db = smem_u32(&sh_sb[ss][j][0]);
 #pragma unroll
           for (int u = 0; u < kBM / 32; ++u) {
             const int r = lane + 32 * u;
@@ -178,9 +184,10 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
                                  : p.scale_b;
             cp_async_4(db + 4 * lane, src, v ? 4u : 0u);
           }
-          cp_async_mbar_arrive(sfull0 + 8 * ss);
+          if (j == KG - 1) cp_async_mbar_arrive(sfull0 + 8 * ss);
         }
       }
+      if (ok && it % KG != 0) cp_async_mbar_arrive(sfull0 + 8 * ((it / KG) % SS));
       cp_async_wait_all();
     }
   } else {
@@ -199,18 +206,18 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
 #pragma unroll
       for (int j = 0; j < C / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const uint32_t ss = it % SS, sph = (it / SS) & 1u;
+        const uint32_t grp = it / KG, ss = grp % SS, sph = (grp / SS) & 1u, j = it % KG;
         const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-        if (!wait_bounded_warp(sfull0 + 8 * ss, sph, abort_flag, p.err) ||
-            !wait_bounded_warp(pf0 + 8 * pb, pph, abort_flag, p.err)) {
+        if ((j == 0 && !wait_bounded_all(sfull0 + 8 * ss, sph, abort_flag, p.err)) ||
+            !wait_bounded_all(pf0 + 8 * pb, pph, abort_flag, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float sa = sh_sa[ss][quarter * 32 + lane];
-        const float sab = B_TILE ? 0.0f : __fmul_rn(sa, sh_sb[ss][wg]);
+        const float sa = sh_sa[ss][j][quarter * 32 + lane];
+        const float sab = B_TILE ? 0.0f : __fmul_rn(sa, sh_sb[ss][j][wg]);
         const float2 sa2 = make_float2(sa, sa);
-        const float *bs = &sh_sb[ss][B_TILE ? wg * C : 0];
+        const float *bs = &sh_sb[ss][j][B_TILE ? wg * C : 0];
 #pragma unroll
         for (int h = 0; h < C / 64; ++h) {
           // 64 columns per round trip: two 32-column TMEM loads, one wait
@@ -258,9 +265,11 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
             }
           }
         }
-        // this K block's scales have been read: hand the slot back
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
+        // the slot's last K block has been read: hand the slot back
+        if (j == KG - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
+        }
       }
       if (!ok) break;
       if (m < p.M) {

@@ -388,5 +388,31 @@ __device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
   return ok != 0;
 }
 
+// Warp-converged variant: every lane polls (one shared-memory operation per
+// poll for the whole warp) and the lanes agree by vote; lane 0 alone checks
+// the abort flag and the clock every 256 polls.
+__device__ __forceinline__ bool wait_bounded_all(uint32_t bar, uint32_t parity,
+                                                 volatile int *abort_flag, unsigned int *err) {
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+    if ((++spins & 255u) == 0) {
+      int verdict = 0;   // 1: another thread aborted, 2: this wait ran out of time
+      if ((threadIdx.x & 31) == 0)
+        verdict = *abort_flag ? 1 : (globaltimer_ns() - t0 > kWaitLimitNs ? 2 : 0);
+      verdict = __shfl_sync(0xFFFFFFFFu, verdict, 0);
+      if (verdict != 0) {
+        if (verdict == 2 && (threadIdx.x & 31) == 0) {
+          *abort_flag = 1;
+          atomicOr(err, 1u);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 }  // namespace ptx
 }  // namespace fp8q

@@ -203,7 +203,9 @@ def test_gemm_exact_when_sums_are_exact(fq):
     assert np.array_equal(f32(y).astype(np.float64), ref)
 
 
-def test_gemm_scale_selects_each_block(fq):
+@pytest.mark.parametrize("M,N,K", [(128, 512, 512), (384, 768, 256), (256, 272, 128),
+                                   (128, 128, 256)])
+def test_gemm_scale_selects_each_block(fq, M, N, K):
     """A's and B's codes all 1.0, a different scale per row and 32-wide block:
     C[m, n] = 32 * sum_j 2^(sa[m, j] - 127) * 2^(sb[n, j] - 127), a closed
     form that pins which scale byte (and which tensor-memory column and lane)
@@ -211,8 +213,9 @@ def test_gemm_scale_selects_each_block(fq):
     multiple of 2^-3 and the sums are exact in fp32: the result must equal the
     closed form bit for bit.  (With terms spread over 2^25 the tensor cores'
     accumulator, which drops addends below the running sum's last place, can
-    land 2.3e-6 low on such an all-positive sum.)"""
-    M, N, K = 128, 512, 512
+    land 2.3e-6 low on such an all-positive sum.)  The shapes cover the
+    one-SM kernel (N <= 128) and the CTA-pair kernel with an odd count of
+    128-row tiles and a ragged last column tile."""
     A = np.full((M, K), 0x38, np.uint8)
     B = np.full((N, K), 0x38, np.uint8)
     rng = np.random.default_rng(12)

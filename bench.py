@@ -958,12 +958,17 @@ def main():
     per_gemm = {}
 
     def timed(name, fn, record=True):
-        """The phase's ms per step; its per-GEMM table goes to per_gemm[name]."""
-        ms = time_steps(torch, dist, stream, fn, K, W, record=run if record else None, clk=clk)
+        """The phase's ms per step, timed with no event inside the steps (an
+        event pair around a launch adds several microseconds to the step);
+        then the same K steps again with an event pair around every GEMM,
+        whose per-GEMM table goes to per_gemm[name]."""
+        ms = time_steps(torch, dist, stream, fn, K, W, clk=clk)
         out = None
-        if record and run.gemm_events:
-            per_gemm[name] = gemm_table(run.gemm_events)
-            out = gemm_summary(run.gemm_events)
+        if record:
+            time_steps(torch, dist, stream, fn, K, 1, record=run, clk=clk)
+            if run.gemm_events:
+                per_gemm[name] = gemm_table(run.gemm_events)
+                out = gemm_summary(run.gemm_events)
         run.gemm_events = None
         return ms, out
 
@@ -1246,7 +1251,8 @@ def main():
                      "kernel": "gemm_tensor_pair_kernel, cta_group::2 (12 GEMMs of the autocast step)",
                      "launches": t_gemm_n, "peak_source": peak_src,
                      "frac_of_sustained": t_gemm_tflops / fp8_peak_sust},
-        "per_gemm": dict(per_gemm, unit="us per launch (CUDA events inside the timed steps)",
+        "per_gemm": dict(per_gemm, unit=("us per launch (CUDA events around each GEMM, in a "
+                                           "repeat of the phase's timed steps)"),
                          peak_tflops=fp8_peak_burst),
         "tiny_linear": tiny,
         "roofline_quantize": {"bound": "hbm", "achieved": tile_gbps, "peak": hbm_peak,

@@ -9,15 +9,32 @@ namespace fp8q {
 namespace gemm {
 namespace {
 
+// Named (hardware) barriers, warp-granular: every thread of the calling warp
+// executes the instruction; `count` is the number of threads that complete one
+// generation.  bar.arrive does not wait; bar.sync waits for the generation.
+__device__ __forceinline__ void nbar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void nbar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------------
 // Tile/block scaled GEMM.  Warpgroup 0 holds the producer (warp 0), the MMA
-// issuer (warp 1) and the scale warp (warp 2); NWG promotion warpgroups
-// follow, warpgroup g owning tile columns [g C, g C + C) with C = BN / NWG.
-// A carries 1x128 tile scales; B carries 128x128 block scales (B_TILE =
-// false) or 1x128 tile scales (B_TILE = true).  Each 128-wide K block is
-// accumulated into one of two TMEM buffers of BN columns; the promotion warps
-// load their C columns of it (64 per round trip), hand the buffer back, and
-// add it into fp32 registers with the block's scale product.  The scales
+// issuer (warp 1), the scale warp (warp 2) and the relay (warp 3); NWG
+// promotion warpgroups follow, warpgroup g owning tile columns [g C, g C + C)
+// with C = BN / NWG.  A carries 1x128 tile scales; B carries 128x128 block
+// scales (B_TILE = false) or 1x128 tile scales (B_TILE = true).  Each
+// 128-wide K block is accumulated into one of two TMEM buffers of BN columns;
+// the promotion warps load their C columns of it (64 per round trip), hand
+// the buffer back, and add it into fp32 registers with the block's scale
+// product.  The handoff runs on named (hardware) barriers: the relay waits
+// for each K block's MMA commit and wakes the promotion warps, and they
+// release the buffer to the MMA warp, so the promotion loop touches no
+// shared-memory barrier on that path (each such operation measured a few
+// hundred cycles while the MMAs stream operands through shared memory).
+// Every role walks the same sequence of K blocks, also after an abort, so
+// the named barriers always balance.  The scales
 // reach them through a shared-memory ring that the scale warp fills with
 // cp.async, kScaleGroup K blocks per slot and kScaleSlots slots ahead, so no
 // global-load latency sits in the promotion loop and its slot handshake
@@ -72,8 +89,8 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
   const uint32_t ring = (raw + 1023u) & ~1023u;
   const uint32_t bars = ring + L::kRingBytes;
   const uint32_t full0 = bars, empty0 = bars + 8 * STAGES;
-  const uint32_t pf0 = bars + 8 * (2 * STAGES), pe0 = pf0 + 16;
-  const uint32_t drain = pe0 + 16;
+  const uint32_t pf0 = bars + 8 * (2 * STAGES);   // MMA commits: buffer b complete
+  const uint32_t drain = pf0 + 32;
   const uint32_t sfull0 = smem_u32(&sh_sbar[0]), sempty0 = sfull0 + 8 * SS;
   const uint32_t slot = bars + L::kBarBytes;
   uint8_t *slot_ptr = smem_raw + (slot - raw);
@@ -87,7 +104,6 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(pf0 + 8 * b, 1);
-      mbar_init(pe0 + 8 * b, NPW);
     }
     for (int s = 0; s < SS; ++s) {
       mbar_init(sfull0 + 8 * s, 32);      // one cp.async arrival per lane of the scale warp
@@ -110,6 +126,16 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(slot_ptr);
   const int total = p.num_m_tiles * p.num_n_tiles;
   const int nkb = p.num_k_blocks;
+  // K blocks this CTA runs (every role walks the same sequence)
+  const uint32_t my_tiles =
+      (int)blockIdx.x < total ? (uint32_t)((total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1) : 0u;
+  const uint32_t T = my_tiles * (uint32_t)nkb;
+  // Named barriers of the MMA -> promotion handoff (id 0 is __syncthreads):
+  //   FULL[b]  the relay arrives, the promotion warps wait: buffer b holds K block it
+  //   RELM[b]  the promotion warps arrive, the MMA warp waits: buffer b may be reused
+  //   ISS[b]   the MMA warp arrives, the relay waits: K block it has been issued
+  constexpr uint32_t kBarFull = 1, kBarRelM = 3, kBarIss = 5;
+  constexpr uint32_t kFullCount = 32u * (1u + NPW), kRelCount = 32u * (NPW + 1u), kIssCount = 64u;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kLowRegs));
@@ -117,26 +143,38 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
       if (lane == 0) producer_loop<BN, STAGES>(&ta, &tb, p, ring, bars, abort_flag);
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) {
-        uint32_t it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
-            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-            const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-            if (!wait_bounded(pe0 + 8 * pb, pph ^ 1u, abort_flag, p.err) ||
-                !wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
-            mma_commit(empty0 + 8 * s);
-            mma_commit(pf0 + 8 * pb);
-          }
+      // MMA issuer.  Before K block it + 2 may overwrite a partial-sum buffer
+      // the promotion warps must have read K block it (RELM); after issuing
+      // K block it it tells the relay warp (ISS).  A failed wait marks the
+      // warp dead: it issues nothing more but keeps every barrier operation,
+      // so the named barriers stay balanced and nothing waits forever.
+      bool dead = false;
+      for (uint32_t it = 0; it < T; ++it) {
+        const uint32_t pb = it & 1u;
+        if (it >= 2) {
+          nbar_sync(kBarRelM + pb, kRelCount);
+          tc_fence_after();
         }
-        drain_mma(drain, abort_flag);
+        if (!dead) {
+          int ok = 1;
+          if (lane == 0) {
+            const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+            ok = wait_bounded(full0 + 8 * s, ph, abort_flag, p.err) ? 1 : 0;
+            if (ok) {
+              tc_fence_after();
+              issue_kblock<BN, STAGES>(ring, s, tmem_base + pb * BN, p.idesc, false);
+              mma_commit(empty0 + 8 * s);
+              mma_commit(pf0 + 8 * pb);
+            }
+          }
+          dead = __shfl_sync(0xFFFFFFFFu, ok, 0) == 0;
+        }
+        __syncwarp();
+        nbar_arrive(kBarIss + pb, kIssCount);
       }
+      // the releases of the last two K blocks complete their generations
+      for (uint32_t k = T >= 2 ? T - 2 : 0; k < T; ++k) nbar_sync(kBarRelM + (k & 1u), kRelCount);
+      if (lane == 0) drain_mma(drain, abort_flag);
       __syncwarp();
     } else if (warp == 2) {
       // Scale warp: every lane copies its share of each K block's scales into
@@ -189,6 +227,18 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
       }
       if (ok && it % KG != 0) cp_async_mbar_arrive(sfull0 + 8 * ((it / KG) % SS));
       cp_async_wait_all();
+    } else {
+      // Relay (warp 3): once K block it is issued (ISS), wait for its MMAs to
+      // complete and wake the promotion warps (FULL) with a named barrier, so
+      // that they never poll a shared-memory barrier on this path.  After an
+      // abort the wait returns at once and the arrivals continue.
+      for (uint32_t it = 0; it < T; ++it) {
+        const uint32_t pb = it & 1u;
+        nbar_sync(kBarIss + pb, kIssCount);
+        if (lane == 0) (void)wait_bounded(pf0 + 8 * pb, (it >> 1) & 1u, abort_flag, p.err);
+        __syncwarp();
+        nbar_arrive(kBarFull + pb, kFullCount);
+      }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kHighRegs));
@@ -196,14 +246,14 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
     const int wg = pw >> 2;
     const int quarter = warp & 3;         // TMEM lane quarter of this warp
     uint32_t it = 0, run_max = 0;
-    // Look-ahead carried from one K block to the next: this lane's early test
-    // of the next accumulator barrier, and the next K block's A scale when it
-    // sits in the same ring slot (read while this K block's FMAs run).
-    uint32_t pf_seen = 0;
+    // Look-ahead carried from one K block to the next: the next K block's A
+    // scale when it sits in the same ring slot (read while this K block's FMAs
+    // run; per-column B scales only).
     float sa_pre = 0.0f;
     bool have_pre = false;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    // Every tile and K block is walked even after an abort, so that the named
+    // barriers stay balanced; nothing is stored then.
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int mt, nt;
       tile_coords(tile, p.num_m_tiles, p.num_n_tiles, mt, nt, kBlockGroupM, 0);
       const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
@@ -213,13 +263,9 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
       for (int j = 0; j < C / 2; ++j) acc2[j] = make_float2(0.0f, 0.0f);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t grp = it / KG, ss = grp % SS, sph = (grp / SS) & 1u, j = it % KG;
-        const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-        if ((j == 0 && !wait_bounded_all(sfull0 + 8 * ss, sph, abort_flag, p.err)) ||
-            (!__all_sync(0xFFFFFFFFu, pf_seen != 0) &&
-             !wait_bounded_all(pf0 + 8 * pb, pph, abort_flag, p.err))) {
-          ok = false;
-          break;
-        }
+        const uint32_t pb = it & 1u;
+        nbar_sync(kBarFull + pb, kFullCount);   // buffer pb holds K block it
+        if (j == 0) (void)wait_bounded_all(sfull0 + 8 * ss, sph, abort_flag, p.err);
         tc_fence_after();
         const float sa = have_pre ? sa_pre : sh_sa[ss][j][quarter * 32 + lane];
         const float sbk = B_TILE ? 0.0f : sh_sb[ss][j][wg];
@@ -237,14 +283,8 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
           tmem_ld_wait();
           if (h == C / 64 - 1) {
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pe0 + 8 * pb);
-            // look ahead to K block it + 1 while the FMAs below issue (with
-            // per-column B scales only: the shorter FMA block of the other
-            // path measured 2% slower with it)
+            nbar_arrive(kBarRelM + pb, kRelCount);   // buffer pb may be overwritten
             if (B_TILE) {
-              const uint32_t nx = it + 1;
-              pf_seen = mbar_test_wait(pf0 + 8 * (nx & 1u), (nx >> 1) & 1u) ? 1u : 0u;
               have_pre = j + 1 < (uint32_t)KG;
               if (have_pre) sa_pre = sh_sa[ss][j + 1][quarter * 32 + lane];
             }
@@ -288,8 +328,7 @@ __global__ void __launch_bounds__(BSConfig<BN, NWG>::kThreads, 1)
           if (lane == 0) mbar_arrive(sempty0 + 8 * ss);
         }
       }
-      if (!ok) break;
-      if (m < p.M) {
+      if (m < p.M && *abort_flag == 0) {
 #pragma unroll
         for (int c = 0; c < C / 32; ++c) {
           const int64_t n0 = ncol0 + c * 32;

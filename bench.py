@@ -79,7 +79,8 @@ PROFILE_CASES = {
 for _rc in ("tensor", "block", "mx"):
     for _ln in ("qkv", "attn_out", "mlp_up", "mlp_down"):
         PROFILE_CASES[f"layer_{_rc}_{_ln}"] = (f"the layer's {_ln} Fprop, Dgrad and Wgrad, "
-                                               f"{_rc} scaling, bf16 out")
+                                               f"{_rc} scaling, bf16 out"
+                                               + (" (one grouped launch)" if _rc == "tensor" else ""))
 
 
 def run_profile_case(case: str):
@@ -118,8 +119,12 @@ def run_profile_case(case: str):
                    (fq.fp8_gemm_dgrad, X(qg, 1, sg), X(qwt, 0, swt)),
                    (fq.fp8_gemm_wgrad, X(qgt, 1, sgt), X(qxt, 0, sxt))]
         del x, w, g
-        for fn, A, B in ops:
-            fn(A, B)
+        if recipe == "tensor":
+            # as the layer step runs them: the linear's three GEMMs in one launch
+            fq.fp8_gemm_grouped([(A, B) for _, A, B in ops])
+        else:
+            for fn, A, B in ops:
+                fn(A, B)
     elif case == "quant_mx_dual":
         x = workloads.normal((16384, 8192), 1.0, 902).cuda()
         for _ in range(3):
@@ -492,6 +497,26 @@ class Runner:
             M, N = C.shape
             self.gemm_events.append((e0, e1, 2.0 * M * N * A.K, (linear, role)))
 
+    def _group(self, o, linear=0):
+        """One linear's Fprop, Dgrad and Wgrad as one fp8_gemm_grouped call."""
+        fq, torch = self.fq, self.torch
+        rec = self.gemm_events is not None
+        if rec:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+        roles = ("fprop", "dgrad", "wgrad")
+        fq.fp8_gemm_grouped([o[r][:2] for r in roles], outs=[o[r][2] for r in roles],
+                            stream=self.stream)
+        if rec:
+            e1.record(self.stream)
+            fl = sum(2.0 * o[r][2].shape[0] * o[r][2].shape[1] * o[r][0].K for r in roles)
+            self.gemm_events.append((e0, e1, fl, (linear, "group")))
+
+    def gemms_grouped(self, ops):
+        for i, o in enumerate(ops):
+            self._group(o, i)
+
     # block recipe ------------------------------------------------------
     def quantize_block(self):
         fq, st = self.fq, self.stream
@@ -574,12 +599,14 @@ class Runner:
                 fq.fp8_amax(L["g"], out=L["ag"], stream=st)
                 fq.fp8_quantize_tensor(L["g"], fq.E5M2, L["ag"], want_q=True, want_qt=True,
                                        q=L["qg"], q_t=L["qgt"], scale=L["tg"], stream=st)
-            for role in ("fprop", "dgrad", "wgrad"):
-                self._gemm(role, *o[role], i)
+            self._group(o, i)    # the linear's three GEMMs in one launch
 
-    tensor_autocast.launches = 4 * 9   # per linear: 3 amax, 3 casts, 3 GEMMs
+    tensor_autocast.launches = 4 * 7   # per linear: 3 amax, 3 casts, 1 grouped GEMM launch
 
     def tensor_prequant(self):
+        self.gemms_grouped(self.tops)
+
+    def tensor_prequant_separate(self):
         self.gemms(self.tops)
 
     # row-wise recipe ----------------------------------------------------
@@ -590,13 +617,12 @@ class Runner:
                 fq.fp8_quantize_rowwise(L[nm], fmt, rows=True, cols=True, q=L["q" + nm],
                                         q_scales=L["r" + nm], q_t=L["q" + nm + "t"],
                                         qt_scales=L["r" + nm + "t"], stream=st)
-            for role in ("fprop", "dgrad", "wgrad"):
-                self._gemm(role, *o[role], i)
+            self._group(o, i)
 
-    row_autocast.launches = 4 * 15   # per linear: 3 x (2 quantize passes + 2 finalizes), 3 GEMMs
+    row_autocast.launches = 4 * 13   # per linear: 3 x (2 quantize passes + 2 finalizes), 1 GEMM group
 
     def row_prequant(self):
-        self.gemms(self.rops)
+        self.gemms_grouped(self.rops)
 
     # end to end: host inputs in, host outputs out --------------------------
     def e2e_host(self):
@@ -948,11 +974,17 @@ def main():
         for (i, role), (ms, n, fl) in sorted(agg.items()):
             us = ms / n * 1e3
             tfl = fl / (us * 1e-6) / 1e12
-            M, N, Kc = [(m, nn, k) for nm, r, m, nn, k in workloads.gemm_problems()
-                        if nm == workloads.LAYER[i].name and r == role][0]
-            rows[f"{workloads.LAYER[i].name}.{role}"] = {
-                "MxNxK": f"{M}x{N}x{Kc}", "us": round(us, 2), "TFLOP/s": round(tfl, 1),
-                "frac": round(tfl / fp8_peak_burst, 3)}
+            nm = workloads.LAYER[i].name
+            if role == "group":
+                shp = ", ".join(f"{m}x{nn}x{k}" for lname, r, m, nn, k in workloads.gemm_problems()
+                                if lname == nm)
+                key, label = f"{nm}.fprop+dgrad+wgrad", shp
+            else:
+                M, N, Kc = [(m, nn, k) for lname, r, m, nn, k in workloads.gemm_problems()
+                            if lname == nm and r == role][0]
+                key, label = f"{nm}.{role}", f"{M}x{N}x{Kc}"
+            rows[key] = {"MxNxK": label, "us": round(us, 2), "TFLOP/s": round(tfl, 1),
+                         "frac": round(tfl / fp8_peak_burst, 3)}
         return rows
 
     per_gemm = {}
@@ -978,6 +1010,9 @@ def main():
         ms_auto, (t_gemm_ms, t_gemm_fl, t_gemm_n) = timed(
             "tensor_current.autocast", lambda: run.tensor_autocast(False))
         ms_pre, _ = timed("tensor_current.prequant", run.tensor_prequant)
+        # the same 12 GEMMs launched one by one, for the per-GEMM table
+        ms_pre_sep, _ = timed("tensor_current.prequant_separate_launches",
+                              run.tensor_prequant_separate)
         ms_d_auto, _ = timed("tensor_delayed_grad.autocast", lambda: run.tensor_autocast(True))
 
         # ---- the same layer with 1x128 / 128x128 scaling
@@ -1151,7 +1186,8 @@ def main():
         "dtype": "fp8->f32",
         "data": "synthetic",
         "config": layer_config(),
-        "prequant": {"value": tf(ms_pre), "unit": "TFLOP/s", "ms_per_step": ms_pre},
+        "prequant": {"value": tf(ms_pre), "unit": "TFLOP/s", "ms_per_step": ms_pre,
+                     "separate_launches_ms_per_step": ms_pre_sep},
         "quantize_ms_per_step": ms_auto - t_gemm_ms / K,
         "delayed_grad": {
             "autocast": {"value": tf(ms_d_auto), "ms_per_step": ms_d_auto}, "unit": "TFLOP/s",
@@ -1248,7 +1284,8 @@ def main():
         "roofline": {"bound": "tensor", "achieved": t_gemm_tflops, "peak": fp8_peak_burst,
                      "unit": "TFLOP/s", "frac": t_gemm_tflops / fp8_peak_burst,
                      "traffic": recorded_traffic("gemm_tensor_pair_kernel"),
-                     "kernel": "gemm_tensor_pair_kernel, cta_group::2 (12 GEMMs of the autocast step)",
+                     "kernel": ("gemm_tensor_pair_kernel, cta_group::2 (the autocast step's 12 "
+                                "GEMMs, each linear's three in one grouped launch)"),
                      "launches": t_gemm_n, "peak_source": peak_src,
                      "frac_of_sustained": t_gemm_tflops / fp8_peak_sust},
         "per_gemm": dict(per_gemm, unit=("us per launch (CUDA events around each GEMM, in a "

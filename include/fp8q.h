@@ -377,6 +377,32 @@ int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw,
                    int out_dtype, int64_t M, int64_t N, int64_t K,
                    cudaStream_t stream);
 
+/* Up to FP8Q_GEMM_GROUP_MAX independent GEMMs in one call, for example one
+ * linear's Fprop, Dgrad and Wgrad ([te_blog] the layer's 12 GEMMs, three per
+ * linear).  Each C_i [M_i, N_i] = A_i [M_i, K_i] . B_i [N_i, K_i]^T is
+ * computed exactly as fp8_gemm computes it, bit for bit.
+ *   When every GEMM has per-tensor or row scales on both operands (the same
+ *   kind across the group), N_i > 128 and no size is 0, the group runs as one
+ *   persistent launch whose output tiles are numbered GEMM after GEMM, so only
+ *   the group's last wave of tiles is partial instead of each GEMM's.
+ *   Otherwise the GEMMs are launched one after another, in order.
+ *   descs: host array of `count` entries (0 <= count <= FP8Q_GEMM_GROUP_MAX);
+ *   every operand is checked as by fp8_gemm, and its scale layout as by the
+ *   role wrappers (the layouts the quantize calls write).  The outputs must
+ *   not overlap one another or any operand.
+ * Errors: as fp8_gemm, for the first GEMM that fails a check (nothing is
+ * launched then); FP8Q_ERR_INVALID_ARG for a count out of range or null
+ * descs. */
+#define FP8Q_GEMM_GROUP_MAX 3
+typedef struct fp8q_gemm_desc {
+  fp8q_operand A;  /* [M, K] */
+  fp8q_operand B;  /* [N, K] */
+  void *C;         /* [M, N], out_dtype */
+  int64_t M, N, K;
+} fp8q_gemm_desc;
+int fp8_gemm_grouped(const fp8q_gemm_desc *descs, int count, int out_dtype,
+                     cudaStream_t stream);
+
 /* ----------------------------------------------------- the whole forward */
 
 /* Bytes of workspace fp8_linear_autocast needs for this recipe and shape

@@ -53,7 +53,8 @@ EXPORTS = (
     "fp8_quantize_tile1x128", "fp8_quantize_rowwise", "fp8_quantize_mxfp8",
     "fp8q_mx_scale_bytes", "fp8_quantize_block128x128", "fp8_gemm",
     "fp8_gemm_amax", "fp8_gemm_fprop",
-    "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8q_linear_workspace_size", "fp8_linear_autocast",
+    "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_grouped", "fp8q_linear_workspace_size",
+    "fp8_linear_autocast",
     "fp8_linear_autocast_noalloc", "fp8q_linear_train_workspace_size", "fp8_linear_train",
     "fp8q_linear_train_host_workspace_size", "fp8_linear_train_host",
 )
@@ -109,6 +110,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_dgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
             "fp8_gemm_wgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+            "fp8_gemm_grouped": (I32, [P, I32, I32, P]),
             "fp8q_linear_workspace_size": (SZ, [I32, I64, I64, I64]),
             "fp8_linear_autocast": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32, P, SZ,
                                           P]),
@@ -399,6 +401,34 @@ class GemmOperand:
     def block_transposed(cls, q_t, fmt, scales):
         """q_t = q^T of a block-quantised matrix; scales as written for q."""
         return cls(q_t, fmt, SCALE_BLOCK_128x128, scales, 1, scales.shape[1])
+
+
+class GemmDesc(ctypes.Structure):
+    """fp8q_gemm_desc: one GEMM of an fp8_gemm_grouped call."""
+    _fields_ = [("A", Operand), ("B", Operand), ("C", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+#: most GEMMs one fp8_gemm_grouped call takes (FP8Q_GEMM_GROUP_MAX)
+GEMM_GROUP_MAX = 3
+
+
+def fp8_gemm_grouped(problems, out_dtype=torch.bfloat16, outs=None, stream=None):
+    """Up to three independent GEMMs in one call: problems = [(A, B), ...]
+    with C_i = A_i . B_i^T as fp8_gemm computes it (one launch when the
+    CTA-pair kernel runs them all).  Returns the outputs."""
+    problems = list(problems)
+    outs = list(outs) if outs is not None else [
+        torch.empty((A.rows, B.rows), dtype=out_dtype, device=A.data.device) for A, B in problems]
+    if len(outs) != len(problems):
+        raise ValueError("one output per problem")
+    arr = (GemmDesc * max(1, len(problems)))()
+    for i, ((A, B), C) in enumerate(zip(problems, outs)):
+        arr[i] = GemmDesc(A.struct, B.struct, _ptr(C), A.rows, B.rows, A.K)
+    dt = _out_dtype(outs[0].dtype) if outs else _out_dtype(out_dtype)
+    _check(lib().fp8_gemm_grouped(ctypes.cast(arr, ctypes.c_void_p), len(problems), dt,
+                                  _stream(stream)), "fp8_gemm_grouped")
+    return outs
 
 
 def _gemm_call(fn_name, A: GemmOperand, B: GemmOperand, out, M, N, K, stream):

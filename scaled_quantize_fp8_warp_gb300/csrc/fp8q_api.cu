@@ -547,6 +547,40 @@ int gemm_role(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dty
 
 }  // namespace
 
+int fp8_gemm_grouped(const fp8q_gemm_desc *descs, int count, int out_dtype,
+                     cudaStream_t stream) {
+  if (count < 0 || count > FP8Q_GEMM_GROUP_MAX || (count > 0 && descs == nullptr) ||
+      !valid_dtype(out_dtype))
+    return FP8Q_ERR_INVALID_ARG;
+  GemmOperandDev A[FP8Q_GEMM_GROUP_MAX], B[FP8Q_GEMM_GROUP_MAX];
+  void *C[FP8Q_GEMM_GROUP_MAX];
+  int64_t M[FP8Q_GEMM_GROUP_MAX], N[FP8Q_GEMM_GROUP_MAX], K[FP8Q_GEMM_GROUP_MAX];
+  for (int i = 0; i < count; ++i) {
+    const fp8q_gemm_desc &d = descs[i];
+    if (d.M < 0 || d.N < 0 || d.K < 0 || d.N % 16 != 0 || d.K % 16 != 0)
+      return FP8Q_ERR_INVALID_ARG;
+    int rc;
+    if ((rc = check_operand(&d.A, d.M, d.K)) != FP8Q_OK) return rc;
+    if ((rc = check_operand(&d.B, d.N, d.K)) != FP8Q_OK) return rc;
+    if ((rc = check_layout(&d.A, d.M, d.K)) != FP8Q_OK) return rc;
+    if ((rc = check_layout(&d.B, d.N, d.K)) != FP8Q_OK) return rc;
+    if (d.M > 0 && d.N > 0) {
+      if (d.C == nullptr) return FP8Q_ERR_INVALID_ARG;
+      if (!aligned16(d.C)) return FP8Q_ERR_MISALIGNED;
+    }
+    A[i] = to_dev(&d.A);
+    B[i] = to_dev(&d.B);
+    C[i] = d.C;
+    M[i] = d.M;
+    N[i] = d.N;
+    K[i] = d.K;
+  }
+  if (count == 0) return FP8Q_OK;
+  int rc;
+  if ((rc = check_device()) != FP8Q_OK) return rc;
+  return launch_gemm_group(A, B, C, M, N, K, count, out_dtype, stream);
+}
+
 int fp8_gemm_fprop(const fp8q_operand *x, const fp8q_operand *w, void *y, int out_dtype,
                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
   // y [M, N] = x [M, K] . w [N, K]^T
@@ -864,6 +898,12 @@ int train_impl(const void *x, const void *w, const void *g, int in_dtype, int64_
     fx.scale = wxt.scale = fp(L.sx);
     fw.scale = dwt.scale = fp(L.sw);
     dg.scale = wgt.scale = fp(L.sg);
+  }
+  if (y_done == nullptr && dx_done == nullptr) {
+    // nobody waits for y or dx alone: the three GEMMs as one group
+    const fp8q_gemm_desc d[3] = {{fx, fw, y, M, N, K}, {dg, dwt, dx, M, K, N},
+                                 {wgt, wxt, dw, N, K, M}};
+    return fp8_gemm_grouped(d, 3, out_dtype, stream);
   }
   if ((rc = fp8_gemm_fprop(&fx, &fw, y, out_dtype, M, N, K, stream)) != FP8Q_OK) return rc;
   if (y_done != nullptr && cudaEventRecord(y_done, stream) != cudaSuccess) return FP8Q_ERR_CUDA;

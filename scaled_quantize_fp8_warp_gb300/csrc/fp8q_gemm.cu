@@ -181,6 +181,40 @@ __global__ void __launch_bounds__(192, 1)
 // both CTAs and hand each CTA's epilogue its half of D; both epilogues
 // release the accumulator on the even CTA's barrier (8 warps).
 // ------------------------------------------------------------------------
+// A group of up to kMaxGroup independent GEMMs (for example a linear's
+// Fprop, Dgrad and Wgrad) run by one persistent launch: their 256 x 256 units
+// are numbered one problem after the other, so only the group's last wave is
+// partial instead of each GEMM's.  A single GEMM is a group of one.
+constexpr int kMaxGroup = 3;
+struct PairGroup {
+  int n;                       // problems in the group
+  int unit_end[kMaxGroup];     // cumulative unit counts
+  GemmArgs prob[kMaxGroup];
+};
+struct PairMaps {
+  CUtensorMap a[kMaxGroup];
+  CUtensorMap b[kMaxGroup];
+};
+
+// The problem of group unit u.  A launch of one GEMM (GROUPED = false) reads
+// problem 0 at constant offsets, as a plain single-GEMM kernel would.
+template <bool GROUPED>
+__device__ __forceinline__ int group_of(const PairGroup &g, int u) {
+  if (!GROUPED) return 0;
+  int q = 0;
+  while (q + 1 < g.n && u >= g.unit_end[q]) ++q;
+  return q;
+}
+
+// Problem q and unit coordinates (unit row mu, column nt) of group unit u.
+template <bool GROUPED>
+__device__ __forceinline__ void group_coords(const PairGroup &g, int u, int &q, int &mu, int &nt) {
+  q = group_of<GROUPED>(g, u);
+  const int lu = u - (q > 0 ? g.unit_end[q - 1] : 0);
+  const GemmArgs &p = g.prob[q];
+  tile_coords(lu, (p.num_m_tiles + 1) / 2, p.num_n_tiles, mu, nt, p.group, p.along_n);
+}
+
 template <int STAGES>
 struct PairLayout {
   static constexpr int kABytes = kBM * kBK;        // this CTA's 128 rows of A
@@ -191,10 +225,10 @@ struct PairLayout {
   static constexpr int kSmemBytes = kRingBytes + kBarBytes + 16 + 1024;
 };
 
-template <int STAGES, int ACC, bool OUT_BF16, bool VEC>
+template <int STAGES, int ACC, bool OUT_BF16, bool VEC, bool GROUPED>
 __global__ void __launch_bounds__(192, 1)
-    gemm_tensor_pair_kernel(const __grid_constant__ CUtensorMap ta,
-                            const __grid_constant__ CUtensorMap tb, const GemmArgs p) {
+    gemm_tensor_pair_kernel(const __grid_constant__ PairMaps maps,
+                            const __grid_constant__ PairGroup g) {
   constexpr int BN = 256;
   using L = PairLayout<STAGES>;
   constexpr uint32_t kTmemCols = ACC * BN;
@@ -212,6 +246,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair's MMAs
+  unsigned int *const err = g.prob[0].err;
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -225,8 +260,10 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
-    prefetch_tmap(&ta);
-    prefetch_tmap(&tb);
+    for (int q = 0; q < (GROUPED ? g.n : 1); ++q) {
+      prefetch_tmap(&maps.a[q]);
+      prefetch_tmap(&maps.b[q]);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(slot, kTmemCols);
@@ -240,10 +277,9 @@ __global__ void __launch_bounds__(192, 1)
   // One allocation serves the pair: both CTAs must hold the same address.
   // Otherwise neither does any work (a symmetric decision, no waiting).
   const bool paired = ld_shared_cluster_u32(mapa_shared(slot, rank ^ 1u)) == tmem_base;
-  if (!paired && threadIdx.x == 0) atomicOr(p.err, 4u);
+  if (!paired && threadIdx.x == 0) atomicOr(err, 4u);
 
-  const int num_mu = (p.num_m_tiles + 1) / 2;
-  const int total = num_mu * p.num_n_tiles;
+  const int total = g.unit_end[GROUPED ? g.n - 1 : 0];
   const int unit0 = blockIdx.x / 2, unit_step = gridDim.x / 2;
 
   if (!paired) {
@@ -252,27 +288,29 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int u = unit0; u < total && ok; u += unit_step) {
-        int mu, nt;
-        tile_coords(u, num_mu, p.num_n_tiles, mu, nt, p.group, p.along_n);
+        int q, mu, nt;
+        group_coords<GROUPED>(g, u, q, mu, nt);
+        const int nkb = g.prob[q].num_k_blocks;
         // past the last M tile (odd count): re-read that tile's A, store nothing
-        const int mt = min(2 * mu + (int)rank, p.num_m_tiles - 1);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+        const int mt = min(2 * mu + (int)rank, g.prob[q].num_m_tiles - 1);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, p.err)) {
+          if (!wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, err)) {
             ok = false;
             break;
           }
           const uint32_t sa = ring + s * L::kStageBytes;
           const uint32_t full_even = mapa_shared(full0 + 8 * s, 0);
           if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * L::kStageBytes);
-          tma_load_2d_pair(sa, &ta, kb * kBK, mt * kBM, full_even);
-          tma_load_2d_pair(sa + L::kABytes, &tb, kb * kBK, nt * BN + (int)rank * 128, full_even);
+          tma_load_2d_pair(sa, &maps.a[q], kb * kBK, mt * kBM, full_even);
+          tma_load_2d_pair(sa + L::kABytes, &maps.b[q], kb * kBK, nt * BN + (int)rank * 128,
+                           full_even);
         }
       }
       // every slot's last release (the even CTA's commits) has arrived here
       for (uint32_t j = 0, jt = it; ok && j < (uint32_t)STAGES; ++j, ++jt)
         ok = wait_bounded(empty0 + 8 * (jt % STAGES), ((jt / STAGES) & 1u) ^ 1u, abort_flag,
-                          p.err);
+                          err);
       if (!ok) {
         // aborting: give copies already issued (their barrier may be the
         // other CTA's) a millisecond to land before the CTA can leave
@@ -289,15 +327,18 @@ __global__ void __launch_bounds__(192, 1)
       for (int u = unit0; u < total && ok; u += unit_step, ++acc_it) {
         const uint32_t buf = ACC == 2 ? (acc_it & 1u) : 0u;
         const uint32_t aph = ACC == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
-        if (!wait_bounded(acce0 + 8 * buf, aph ^ 1u, abort_flag, p.err)) {
+        if (!wait_bounded(acce0 + 8 * buf, aph ^ 1u, abort_flag, err)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb, ++it) {
+        const int q = group_of<GROUPED>(g, u);
+        const int nkb = g.prob[q].num_k_blocks;
+        const uint32_t idesc = g.prob[q].idesc;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!wait_bounded(full0 + 8 * s, ph, abort_flag, p.err)) {
+          if (!wait_bounded(full0 + 8 * s, ph, abort_flag, err)) {
             ok = false;
             break;
           }
@@ -307,7 +348,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k) {
             const uint64_t ad = sdesc_k(a0 + k * kUmmaK, kSwzSBO, kSwzMode);
             const uint64_t bd = sdesc_k(b0 + k * kUmmaK, kSwzSBO, kSwzMode);
-            mma_f8f6f4_pair(d_tmem, ad, bd, p.idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            mma_f8f6f4_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit_pair_multicast(empty0 + 8 * s, kBoth);
         }
@@ -324,16 +365,20 @@ __global__ void __launch_bounds__(192, 1)
     // Epilogue warps 2..5 -> TMEM lane quarters 2, 3, 0, 1 of this CTA's
     // 128 rows of the pair tile.
     const int quarter = warp & 3;
-    const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
     const uint32_t acce_even0 = mapa_shared(acce0, 0);
-    uint32_t acc_it = 0, run_max = 0;
+    uint32_t acc_it = 0, run_max0 = 0, run_max1 = 0, run_max2 = 0;   // per problem
     for (int u = unit0; u < total; u += unit_step, ++acc_it) {
-      int mu, nt;
-      tile_coords(u, num_mu, p.num_n_tiles, mu, nt, p.group, p.along_n);
+      int q, mu, nt;
+      group_coords<GROUPED>(g, u, q, mu, nt);
+      // this unit's problem, read from the parameter block once (a reference
+      // into it would be re-read after every asm statement)
+      const GemmArgs p = g.prob[q];
+      const float scale = VEC ? 0.0f : __fmul_rn(p.scale_a[0], p.scale_b[0]);
+      uint32_t run_max = 0;
       const int mt = 2 * mu + (int)rank;   // >= num_m_tiles: nothing to store
       const uint32_t buf = ACC == 2 ? (acc_it & 1u) : 0u;
       const uint32_t aph = ACC == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
-      if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, p.err)) break;
+      if (!wait_bounded_warp(accf0 + 8 * buf, aph, abort_flag, err)) break;
       tc_fence_after();
       const int64_t m = (int64_t)mt * kBM + quarter * 32 + lane;
       float sa = 0.0f;
@@ -359,6 +404,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (m < p.M && n0 < p.N) run_max = max(run_max, store32<OUT_BF16>(p.C, p.N, m, n0, v));
       }
+      if (q == 0) run_max0 = max(run_max0, run_max);
+      else if (q == 1) run_max1 = max(run_max1, run_max);
+      else run_max2 = max(run_max2, run_max);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -368,7 +416,9 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_cluster(acce_even0 + 8 * buf);
       }
     }
-    publish_amax(p.amax, run_max);
+    publish_amax(g.prob[0].amax, run_max0);
+    if (GROUPED && g.n > 1) publish_amax(g.prob[1].amax, run_max1);
+    if (GROUPED && g.n > 2) publish_amax(g.prob[2].amax, run_max2);
   }
 
   tc_fence_before();
@@ -378,11 +428,10 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-template <int STAGES, int ACC, bool OUT_BF16, bool VEC>
-int run_tensor_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
-                    cudaStream_t stream) {
+template <int STAGES, int ACC, bool OUT_BF16, bool VEC, bool GROUPED>
+int run_tensor_pair(const PairMaps &maps, const PairGroup &grp, cudaStream_t stream) {
   using L = PairLayout<STAGES>;
-  auto kernel = gemm_tensor_pair_kernel<STAGES, ACC, OUT_BF16, VEC>;
+  auto kernel = gemm_tensor_pair_kernel<STAGES, ACC, OUT_BF16, VEC, GROUPED>;
   static bool attr_done = false;  // per instantiation
   static int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
@@ -404,12 +453,33 @@ int run_tensor_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs
       return FP8Q_ERR_CUDA;
     attr_done = true;
   }
-  GemmArgs pa = a;
-  pa.idesc = ptx::idesc_f8f6f4((a.idesc >> 7) & 7u, (a.idesc >> 10) & 7u, 256, 256);
-  const int units = ((a.num_m_tiles + 1) / 2) * a.num_n_tiles;
+  const int units = grp.unit_end[grp.n - 1];
+  if (units <= 0) return FP8Q_OK;
   cfg.gridDim = dim3(2 * (units < max_clusters ? units : max_clusters), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kernel, ta, tb, pa) != cudaSuccess) return FP8Q_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kernel, maps, grp) != cudaSuccess) return FP8Q_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
+}
+
+// One problem of a pair group: the pair instruction descriptor (M = N = 256)
+// and the problem's unit count.
+void add_pair_problem(PairMaps &maps, PairGroup &grp, const CUtensorMap &ta,
+                      const CUtensorMap &tb, const GemmArgs &a) {
+  const int q = grp.n++;
+  maps.a[q] = ta;
+  maps.b[q] = tb;
+  grp.prob[q] = a;
+  grp.prob[q].idesc = ptx::idesc_f8f6f4((a.idesc >> 7) & 7u, (a.idesc >> 10) & 7u, 256, 256);
+  const int units = ((a.num_m_tiles + 1) / 2) * a.num_n_tiles;
+  grp.unit_end[q] = (q > 0 ? grp.unit_end[q - 1] : 0) + units;
+}
+
+template <int STAGES, int ACC, bool OUT_BF16, bool VEC>
+int run_tensor_pair(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a,
+                    cudaStream_t stream) {
+  PairMaps maps;
+  PairGroup grp{};
+  add_pair_problem(maps, grp, ta, tb, a);
+  return run_tensor_pair<STAGES, ACC, OUT_BF16, VEC, false>(maps, grp, stream);
 }
 
 template <int BN, int STAGES, bool OUT_BF16, bool VEC>
@@ -427,6 +497,16 @@ int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, 
 }
 
 }  // namespace
+
+int run_tensor_pair_group(const PairMaps &maps, const PairGroup &grp, bool bf16, bool vec,
+                          cudaStream_t stream) {
+  constexpr int PS = kPairStages, PA = kPairAcc;
+  if (vec)
+    return bf16 ? run_tensor_pair<PS, PA, true, true, true>(maps, grp, stream)
+                : run_tensor_pair<PS, PA, false, true, true>(maps, grp, stream);
+  return bf16 ? run_tensor_pair<PS, PA, true, false, true>(maps, grp, stream)
+              : run_tensor_pair<PS, PA, false, false, true>(maps, grp, stream);
+}
 
 int run_tensor_family(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
                       int BN, bool bf16, bool vec, cudaStream_t stream) {
@@ -520,6 +600,32 @@ bool make_tmap_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dtype, u
   return r == CUDA_SUCCESS;
 }
 
+// The launch arguments every kernel family shares.
+static void fill_args(GemmArgs &a, const GemmOperandDev &A, const GemmOperandDev &B, void *C,
+                      int64_t M, int64_t N, int64_t K, int BN, float *amax_out) {
+  a = GemmArgs{};
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.num_m_tiles = (int)((M + kBM - 1) / kBM);
+  a.num_n_tiles = (int)((N + BN - 1) / BN);
+  a.num_k_blocks = (int)((K + kBK - 1) / kBK);
+  a.idesc = ptx::idesc_f8f6f4((uint32_t)A.format, (uint32_t)B.format, kBM, (uint32_t)BN);
+  a.C = C;
+  a.scale_a = A.scale;
+  a.scale_b = B.scale;
+  a.a_stride_row = A.stride_row;
+  a.a_stride_k = A.stride_k;
+  a.b_stride_row = B.stride_row;
+  a.b_stride_k = B.stride_k;
+  a.a_row = A.scaling == FP8Q_SCALE_ROW ? 1 : 0;
+  a.b_row = B.scaling == FP8Q_SCALE_ROW ? 1 : 0;
+  a.amax = reinterpret_cast<unsigned int *>(amax_out);
+  a.mx_a = A.mx_scale;
+  a.mx_b = B.mx_scale;
+  a.err = device_error_word();
+}
+
 int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int out_dtype,
                 int64_t M, int64_t N, int64_t K, cudaStream_t stream, float *amax_out) {
   const bool bf16 = out_dtype == FP8Q_DT_BF16;
@@ -550,27 +656,8 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
       !make_tmap(&tb, B.data, (uint64_t)N, (uint64_t)K, (uint32_t)b_box_rows))
     return FP8Q_ERR_CUDA;
 
-  GemmArgs a{};
-  a.M = M;
-  a.N = N;
-  a.K = K;
-  a.num_m_tiles = (int)((M + kBM - 1) / kBM);
-  a.num_n_tiles = (int)((N + BN - 1) / BN);
-  a.num_k_blocks = (int)((K + kBK - 1) / kBK);
-  a.idesc = ptx::idesc_f8f6f4((uint32_t)A.format, (uint32_t)B.format, kBM, (uint32_t)BN);
-  a.C = C;
-  a.scale_a = A.scale;
-  a.scale_b = B.scale;
-  a.a_stride_row = A.stride_row;
-  a.a_stride_k = A.stride_k;
-  a.b_stride_row = B.stride_row;
-  a.b_stride_k = B.stride_k;
-  a.a_row = A.scaling == FP8Q_SCALE_ROW ? 1 : 0;
-  a.b_row = B.scaling == FP8Q_SCALE_ROW ? 1 : 0;
-  a.amax = reinterpret_cast<unsigned int *>(amax_out);
-  a.mx_a = A.mx_scale;
-  a.mx_b = B.mx_scale;
-  a.err = device_error_word();
+  GemmArgs a;
+  fill_args(a, A, B, C, M, N, K, BN, amax_out);
   if (a.err == nullptr) return FP8Q_ERR_CUDA;
   const int64_t tiles = (int64_t)a.num_m_tiles * a.num_n_tiles;
   if (tiles > INT32_MAX / 2) return FP8Q_ERR_INVALID_ARG;
@@ -594,6 +681,49 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   }
   return run_blockscaled_family(ta, tb, a, grid, bf16, B.scaling == FP8Q_SCALE_TILE_1x128,
                                 stream);
+}
+
+int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *const *C,
+                      const int64_t *M, const int64_t *N, const int64_t *K, int count,
+                      int out_dtype, cudaStream_t stream) {
+  // One launch when every problem runs on the CTA-pair kernel (per-tensor or
+  // row scales, N > 128, nothing empty) with the same scaling kind.
+  bool pair = count >= 1 && count <= kMaxGroup;
+  bool vec0 = false;
+  for (int i = 0; i < count && pair; ++i) {
+    const bool a_ep = A[i].scaling == FP8Q_SCALE_TENSOR || A[i].scaling == FP8Q_SCALE_ROW;
+    const bool b_ep = B[i].scaling == FP8Q_SCALE_TENSOR || B[i].scaling == FP8Q_SCALE_ROW;
+    const bool vec = A[i].scaling == FP8Q_SCALE_ROW || B[i].scaling == FP8Q_SCALE_ROW;
+    if (!a_ep || !b_ep || N[i] <= 128 || M[i] == 0 || K[i] == 0) pair = false;
+    if (i == 0)
+      vec0 = vec;
+    else if (vec != vec0)
+      pair = false;
+  }
+  if (!pair) {
+    for (int i = 0; i < count; ++i) {
+      const int rc = launch_gemm(A[i], B[i], C[i], out_dtype, M[i], N[i], K[i], stream, nullptr);
+      if (rc != FP8Q_OK) return rc;
+    }
+    return FP8Q_OK;
+  }
+  PairMaps maps;
+  PairGroup grp{};
+  int64_t units = 0;
+  for (int i = 0; i < count; ++i) {
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A[i].data, (uint64_t)M[i], (uint64_t)K[i], kBM) ||
+        !make_tmap(&tb, B[i].data, (uint64_t)N[i], (uint64_t)K[i], 128))
+      return FP8Q_ERR_CUDA;
+    GemmArgs a;
+    fill_args(a, A[i], B[i], C[i], M[i], N[i], K[i], 256, nullptr);
+    if (a.err == nullptr) return FP8Q_ERR_CUDA;
+    units += (int64_t)((a.num_m_tiles + 1) / 2) * a.num_n_tiles;
+    if (units > INT32_MAX / 2) return FP8Q_ERR_INVALID_ARG;
+    raster_for((a.num_m_tiles + 1) / 2, a.num_n_tiles, 256, 256, K[i], a.group, a.along_n);
+    add_pair_problem(maps, grp, ta, tb, a);
+  }
+  return run_tensor_pair_group(maps, grp, out_dtype == FP8Q_DT_BF16, vec0, stream);
 }
 
 }  // namespace fp8q

@@ -90,4 +90,10 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C,
                 int out_dtype, int64_t M, int64_t N, int64_t K,
                 cudaStream_t stream, float *amax_out = nullptr);
 
+// Independent GEMMs (count <= 3) in one launch where the CTA-pair kernel runs
+// them all, else one launch each; arguments already validated.
+int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *const *C,
+                      const int64_t *M, const int64_t *N, const int64_t *K, int count,
+                      int out_dtype, cudaStream_t stream);
+
 }  // namespace fp8q

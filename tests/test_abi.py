@@ -69,14 +69,16 @@ def test_struct_sizes_match_header(tmp_path, lib):
     import scaled_quantize_fp8_warp_gb300 as fq
     src = tmp_path / "sz.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "fp8q.h"\n'
-                   'int main(void){printf("%zu %zu %zu %zu\\n", sizeof(fp8q_amax_history),'
+                   'int main(void){printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(fp8q_amax_history),'
                    ' sizeof(fp8q_operand), offsetof(fp8q_amax_history, next),'
-                   ' offsetof(fp8q_operand, scale_stride_row));return 0;}\n')
+                   ' offsetof(fp8q_operand, scale_stride_row), sizeof(fp8q_gemm_desc),'
+                   ' offsetof(fp8q_gemm_desc, K));return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include",
                     str(src), "-o", str(exe)], check=True)
-    hist, op, nxt, srow = map(int, subprocess.run([str(exe)], capture_output=True, text=True,
-                                                  check=True).stdout.split())
+    hist, op, nxt, srow, gd, gdk = map(int, subprocess.run([str(exe)], capture_output=True,
+                                                           text=True, check=True).stdout.split())
+    assert gd == ctypes.sizeof(fq.GemmDesc) and gdk == fq.GemmDesc.K.offset
     assert hist == fq.HISTORY_BYTES and nxt == 4 * fq.HISTORY_LEN
     assert op == ctypes.sizeof(fq.Operand)
     assert srow == fq.Operand.scale_stride_row.offset
@@ -197,6 +199,43 @@ def test_role_wrappers_reject_undocumented_scale_layouts(lib):
                               None) == 6
     assert lib.fp8_gemm_wgrad(ctypes.byref(xt2), ctypes.byref(gt), y, fq.DT_BF16, M, N, K,
                               None) == 1
+
+
+def test_grouped_gemm_validation_before_device(lib):
+    """fp8_gemm_grouped: a count outside [0, 3] or null descriptors are
+    INVALID_ARG (1); count 0 does nothing (OK, 0); every descriptor is checked
+    like the role wrappers check theirs (an undocumented scale stride is 1)
+    before any device work.  These cases never reach a launch."""
+    import scaled_quantize_fp8_warp_gb300 as fq
+    P = ctypes.c_void_p
+    assert lib.fp8_gemm_grouped(None, 0, fq.DT_BF16, None) == 0
+    assert lib.fp8_gemm_grouped(None, 1, fq.DT_BF16, None) == 1
+    M, N, K = 256, 384, 512
+    ten = fq.Operand(0x10000, fq.E4M3, fq.SCALE_TENSOR, 0x20000, 0, 0)
+    badtile = fq.Operand(0x10000, fq.E4M3, fq.SCALE_TILE_1x128, 0x20000, 1, M - 16)
+    arr = (fq.GemmDesc * 4)()
+    for i in range(4):
+        arr[i] = fq.GemmDesc(ten, ten, 0x40000, M, N, K)
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, P), 4, fq.DT_BF16, None) == 1
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, P), -1, fq.DT_BF16, None) == 1
+    arr[1] = fq.GemmDesc(badtile, ten, 0x40000, M, N, K)
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, P), 3, fq.DT_BF16, None) == 1
+    arr[1] = fq.GemmDesc(ten, ten, 0x40000, M, N + 8, K)      # N % 16 != 0
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, P), 3, fq.DT_BF16, None) == 1
+    arr[1] = fq.GemmDesc(ten, ten, 0x40008, M, N, K)          # C not 16-byte aligned
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, P), 3, fq.DT_BF16, None) == 2
+
+
+@pytest.mark.skipif(_has_cuda_device(),
+                    reason="valid descriptors would reach a kernel launch on placeholder pointers")
+def test_grouped_gemm_valid_descriptors_reach_the_device_check(lib):
+    import scaled_quantize_fp8_warp_gb300 as fq
+    M, N, K = 256, 384, 512
+    ten = fq.Operand(0x10000, fq.E4M3, fq.SCALE_TENSOR, 0x20000, 0, 0)
+    arr = (fq.GemmDesc * 3)()
+    for i in range(3):
+        arr[i] = fq.GemmDesc(ten, ten, 0x40000, M, N, K)
+    assert lib.fp8_gemm_grouped(ctypes.cast(arr, ctypes.c_void_p), 3, fq.DT_BF16, None) == 6
 
 
 def test_linear_sizes_that_overflow_are_rejected(lib):

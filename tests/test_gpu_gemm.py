@@ -592,3 +592,77 @@ def test_gemm_fused_amax_full_size_qkv_fprop(fq):
     assert_f32_bits_equal(f32(am), f32(ref), "fused amax")
     assert_f32_bits_equal(f32(am), np.array([oracle.amax(to_oracle(y))], np.float32),
                           "fused amax vs oracle")
+
+
+def _rand_fp8(shape, fmt, seed):
+    """Random finite FP8 codes (no NaN/Inf) as a uint8 device tensor."""
+    g = torch.Generator().manual_seed(seed)
+    v = torch.randn(shape, generator=g) * (4.0 if fmt == 0 else 64.0)
+    dt = torch.float8_e4m3fn if fmt == 0 else torch.float8_e5m2
+    return v.to(dt).view(torch.uint8).cuda()
+
+
+@pytest.mark.parametrize("kind", ["tensor", "row"])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_grouped_equals_separate_calls(fq, kind, out_dtype):
+    """fp8_gemm_grouped runs a linear's three GEMMs as one launch; every
+    output must equal the separate fp8_gemm call bit for bit.  Shapes with an
+    odd number of 128-row tiles, a ragged last column tile and three
+    different contractions."""
+    M, N, K = 400, 272, 336            # Fprop [M, N] over K; Dgrad [M, K] over N; Wgrad [N, K] over M
+    probs = [(M, N, K), (M, K, N), (N, K, M)]
+    fmts = [(0, 0), (1, 0), (1, 0)]
+    ops = []
+    for i, ((m, n, k), (fa, fb)) in enumerate(zip(probs, fmts)):
+        a, b = _rand_fp8((m, k), fa, 100 + i), _rand_fp8((n, k), fb, 200 + i)
+        if kind == "tensor":
+            sa = torch.tensor([0.75 + 0.1 * i], device="cuda")
+            sb = torch.tensor([1.5 - 0.2 * i], device="cuda")
+            A, B = fq.GemmOperand.tensor(a, fa, sa), fq.GemmOperand.tensor(b, fb, sb)
+        else:
+            g = torch.Generator().manual_seed(300 + i)
+            sa = (torch.rand(m, generator=g) + 0.5).cuda()
+            sb = (torch.rand(n, generator=g) + 0.5).cuda()
+            A, B = fq.GemmOperand.row(a, fa, sa), fq.GemmOperand.row(b, fb, sb)
+        ops.append((A, B))
+    grouped = fq.fp8_gemm_grouped(ops, out_dtype=out_dtype)
+    gpu_status_ok(fq)
+    for i, (A, B) in enumerate(ops):
+        sep = fq.fp8_gemm(A, B, out_dtype=out_dtype)
+        gpu_status_ok(fq)
+        assert torch.equal(grouped[i].view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32),
+                           sep.view(torch.int16 if out_dtype == torch.bfloat16 else torch.int32)), i
+
+
+def test_grouped_layer_linear_full_size(fq):
+    """The attention-out linear at full size (15872 tokens), per-tensor
+    scaling: the grouped launch equals the three role calls bit for bit."""
+    shape = workloads.LAYER[1]
+    x, w, g = (t.cuda() for t in workloads.layer_inputs(shape, 1))
+    qx, qxt, sx = fq.fp8_quantize_tensor(x, 0, fq.fp8_amax(x), want_qt=True)
+    qw, qwt, sw = fq.fp8_quantize_tensor(w, 0, fq.fp8_amax(w), want_qt=True)
+    qg, qgt, sg = fq.fp8_quantize_tensor(g, 1, fq.fp8_amax(g), want_qt=True)
+    T = fq.GemmOperand.tensor
+    ops = [(T(qx, 0, sx), T(qw, 0, sw)), (T(qg, 1, sg), T(qwt, 0, sw)), (T(qgt, 1, sg), T(qxt, 0, sx))]
+    grouped = fq.fp8_gemm_grouped(ops)
+    sep = [fq.fp8_gemm_fprop(*ops[0]), fq.fp8_gemm_dgrad(*ops[1]), fq.fp8_gemm_wgrad(*ops[2])]
+    gpu_status_ok(fq)
+    for i in range(3):
+        assert torch.equal(grouped[i].view(torch.int16), sep[i].view(torch.int16)), i
+
+
+def test_grouped_falls_back_for_other_scalings(fq):
+    """A group the pair kernel cannot run (1x128 tiles with 128x128 blocks,
+    N <= 128) runs one launch per GEMM; results still equal separate calls."""
+    M, N, K = 256, 384, 256
+    a, b = _rand_fp8((M, K), 0, 7), _rand_fp8((N, K), 0, 8)
+    qa, sa, _, _ = fq.fp8_quantize_tile1x128(a.view(torch.float8_e4m3fn).float().to(torch.bfloat16), 0)
+    qb, _, sb = fq.fp8_quantize_block128x128(b.view(torch.float8_e4m3fn).float().to(torch.bfloat16), 0)
+    t1 = (fq.GemmOperand.tile(qa, 0, sa), fq.GemmOperand.block(qb, 0, sb))
+    c, d = _rand_fp8((M, K), 0, 9), _rand_fp8((128, K), 0, 10)
+    one = torch.ones(1, device="cuda")
+    t2 = (fq.GemmOperand.tensor(c, 0, one), fq.GemmOperand.tensor(d, 0, one))
+    grouped = fq.fp8_gemm_grouped([t1, t2], out_dtype=torch.float32)
+    gpu_status_ok(fq)
+    for i, (A, B) in enumerate([t1, t2]):
+        assert torch.equal(grouped[i], fq.fp8_gemm(A, B, out_dtype=torch.float32)), i

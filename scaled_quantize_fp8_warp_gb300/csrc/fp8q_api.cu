@@ -899,12 +899,6 @@ int train_impl(const void *x, const void *w, const void *g, int in_dtype, int64_
     fw.scale = dwt.scale = fp(L.sw);
     dg.scale = wgt.scale = fp(L.sg);
   }
-  if (y_done == nullptr && dx_done == nullptr) {
-    // nobody waits for y or dx alone: the three GEMMs as one group
-    const fp8q_gemm_desc d[3] = {{fx, fw, y, M, N, K}, {dg, dwt, dx, M, K, N},
-                                 {wgt, wxt, dw, N, K, M}};
-    return fp8_gemm_grouped(d, 3, out_dtype, stream);
-  }
   if ((rc = fp8_gemm_fprop(&fx, &fw, y, out_dtype, M, N, K, stream)) != FP8Q_OK) return rc;
   if (y_done != nullptr && cudaEventRecord(y_done, stream) != cudaSuccess) return FP8Q_ERR_CUDA;
   if ((rc = fp8_gemm_dgrad(&dg, &dwt, dx, out_dtype, M, N, K, stream)) != FP8Q_OK) return rc;

@@ -498,10 +498,10 @@ int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, 
 
 }  // namespace
 
-int run_tensor_pair_group(const PairMaps &maps, const PairGroup &grp, bool bf16, bool vec,
+// A group of per-tensor-scaled problems (row scales are never grouped).
+int run_tensor_pair_group(const PairMaps &maps, const PairGroup &grp, bool bf16,
                           cudaStream_t stream) {
   constexpr int PS = kPairStages, PA = kPairAcc;
-  if (vec) return FP8Q_ERR_NOT_IMPLEMENTED;   // row scales are never grouped
   return bf16 ? run_tensor_pair<PS, PA, true, false, true>(maps, grp, stream)
               : run_tensor_pair<PS, PA, false, false, true>(maps, grp, stream);
 }
@@ -689,7 +689,6 @@ int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *co
   // grouped form of their per-element scale epilogue measured 17% slower on
   // the layer's GEMMs.
   bool pair = count >= 1 && count <= kMaxGroup;
-  const bool vec0 = false;
   for (int i = 0; i < count && pair; ++i) {
     if (A[i].scaling != FP8Q_SCALE_TENSOR || B[i].scaling != FP8Q_SCALE_TENSOR || N[i] <= 128 ||
         M[i] == 0 || K[i] == 0)
@@ -718,7 +717,7 @@ int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *co
     raster_for((a.num_m_tiles + 1) / 2, a.num_n_tiles, 256, 256, K[i], a.group, a.along_n);
     add_pair_problem(maps, grp, ta, tb, a);
   }
-  return run_tensor_pair_group(maps, grp, out_dtype == FP8Q_DT_BF16, vec0, stream);
+  return run_tensor_pair_group(maps, grp, out_dtype == FP8Q_DT_BF16, stream);
 }
 
 }  // namespace fp8q

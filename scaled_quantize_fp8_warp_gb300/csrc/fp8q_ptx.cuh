@@ -45,19 +45,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of the same condition as mbar_try_wait.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred P1;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, P1;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -291,18 +278,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 
-// 32 lanes x 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -311,22 +286,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) swizzle atoms
 // stacked along M/N.  Fields: start address >> 4 in [0,14), leading byte
 // offset >> 4 in [16,30) (unused for this layout; 16 bytes), stride byte
-// offset >> 4 in [32,46) (1024 bytes between 8-row groups), the fixed value
-// 0b001 in [46,49), base offset 0 (atoms 1024-byte aligned), swizzle mode 2
-// (128-byte) in [61,64).
-__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(16u >> 4) << 16;
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
-}
-
-// The same for a swizzle mode / 8-row stride given explicitly (mode 2 with
-// 1024-byte SBO: 128-byte swizzle; mode 4 with 512-byte SBO: 64-byte
-// swizzle, rows of 64 bytes).
+// offset >> 4 in [32,46) (`sbo` bytes between 8-row groups), the fixed value
+// 0b001 in [46,49), base offset 0 (atoms 1024-byte aligned), swizzle mode
+// in [61,64): mode 2 with a 1024-byte stride is the 128-byte swizzle, mode 4
+// with a 512-byte stride the 64-byte swizzle (rows of 64 bytes).
 __device__ __forceinline__ uint64_t sdesc_k(uint32_t saddr, uint32_t sbo, uint32_t mode) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);

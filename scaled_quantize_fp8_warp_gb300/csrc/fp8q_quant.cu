@@ -412,7 +412,6 @@ template <typename InT>
 struct QuantRing {
   static constexpr int kTileBytes = 128 * 128 * (int)sizeof(InT);
   static constexpr int kStages = sizeof(InT) == 2 ? 3 : 2;
-  static constexpr int kSmemBytes = kStages * kTileBytes + 1024;  // + alignment slack
 };
 
 #ifndef FP8Q_QUANT_MINB3

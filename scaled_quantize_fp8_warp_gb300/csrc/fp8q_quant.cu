@@ -414,9 +414,6 @@ struct QuantRing {
   static constexpr int kStages = sizeof(InT) == 2 ? 3 : 2;
 };
 
-#ifndef FP8Q_QUANT_MINB3
-#define FP8Q_QUANT_MINB3 1
-#endif
 // CTAs per SM a mode is built for: bf16 input runs three CTAs of two-stage
 // rings (the same tiles in flight per SM as two CTAs of three stages, with 50%
 // more warps to hide the cast's latency; every mode fits 85 registers without
@@ -426,16 +423,16 @@ struct QuantRing {
 template <typename InT, int KM>
 struct QuantShape {
   // modes that can write the transposed copy stage it through shared memory
-  static constexpr bool kStaging = !(KM == 2 || KM == 6);
+  static constexpr bool kStaging = !(KM == kKTileRow || KM == kKRowAmax);
   static constexpr int kStageBytes = kStaging ? 64 * 128 : 0;
   // the column-tile modes' own scratch would not leave room for three
-  static constexpr bool kThree = FP8Q_QUANT_MINB3 != 0 && sizeof(InT) == 2 &&
-                                 !(KM == 3 || KM == 4 || KM == 7 || KM == 9);
+  static constexpr bool kThree = sizeof(InT) == 2 && !(KM == kKTileCol || KM == kKTileBoth ||
+                                                       KM == kKRowCast || KM == kKMx);
   static constexpr int kMinBlocks = kThree ? 3 : 2;
   static constexpr int kStages = kThree ? 2 : QuantRing<InT>::kStages;
   static constexpr int kTileBytes = QuantRing<InT>::kTileBytes;
   // MXFP8: the tile's two 512-byte scale atoms are assembled in shared memory
-  static constexpr int kMxBytes = KM == 9 ? 1024 : 0;
+  static constexpr int kMxBytes = KM == kKMx ? 1024 : 0;
   static constexpr int kSmemBytes = kStages * kTileBytes + kStageBytes + kMxBytes + 1024;
 };
 

@@ -1,0 +1,89 @@
+"""Host logic of bench.py that needs no GPU: the clock record of a timed
+region (nvidia-smi samples kept only inside the region's wall-clock window)
+and the rule that voids a number measured under a slowdown or a clock lock,
+and the guard that reports DRAM traffic only for unchanged kernel sources."""
+import datetime
+import json
+
+import bench
+
+UUID = "GPU-0000"
+
+
+def _line(t, sm, smax=2070, reasons=("Not Active",) * 4, uuid=UUID, power=1300.0):
+    stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    active = "0x0000000000000004" if "Active" in reasons else "0x0000000000000000"
+    return ", ".join([stamp, uuid, str(sm), str(smax), f"{power:.2f}", active, *reasons])
+
+
+def _sampler(lines, windows):
+    s = bench.ClockSampler(UUID)
+    s.lines = list(lines)
+    s.windows = list(windows)
+    return s
+
+
+def test_summary_keeps_samples_inside_the_windows_only():
+    t0 = 1_700_000_000.0
+    lines = [_line(t0 + 0.05 * i, 1000 if i < 10 else 1900) for i in range(30)]
+    lines.append(_line(t0 + 0.6, 100, uuid="GPU-other"))      # another GPU's sample
+    s = _sampler(lines, [(t0 + 0.5, t0 + 1.2)])
+    out = s.summary()
+    assert out["sm_mhz"] == 1900.0
+    assert out["sm_max_mhz"] == 2070.0
+    assert out["samples_in_timed_regions"] == 15
+    assert out["reasons"] == []
+    # an explicit window list overrides the recorded one
+    early = s.summary(windows=[(t0, t0 + 0.45)], span="early")
+    assert early["sm_mhz"] == 1000.0 and early["span"] == "early"
+
+
+def test_summary_collects_active_reasons():
+    t0 = 1_700_000_000.0
+    cap = ("Not Active", "Not Active", "Not Active", "Active")
+    thermal = ("Not Active", "Active", "Not Active", "Not Active")
+    lines = [_line(t0 + 0.05 * i, 1850, reasons=cap) for i in range(10)]
+    lines.append(_line(t0 + 0.2, 1500, reasons=thermal))
+    out = _sampler(lines, [(t0, t0 + 1.0)]).summary()
+    assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_rejection_rule():
+    ok = {"sm_mhz": 1852.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert bench.clock_rejection(ok) == []
+    # a power cap explains a lower clock: the number stands
+    assert bench.clock_rejection({**ok, "sm_mhz": 1200.0}) == []
+    for r in bench.REJECTING_REASONS:
+        assert bench.clock_rejection({**ok, "reasons": ["sw_power_cap", r]}) == [r]
+    # a low clock with no reason reported reads as a leftover clock lock
+    locked = {"sm_mhz": 1100.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert len(bench.clock_rejection(locked)) == 1
+    assert bench.clock_rejection({**locked, "sm_mhz": 2000.0}) == []
+    # no samples at all voids nothing (and says so in the record itself)
+    assert bench.clock_rejection({"sm_mhz": None, "sm_max_mhz": None,
+                                  "reasons": ["unsampled"]}) == []
+
+
+def test_recorded_traffic_follows_the_source_digest(tmp_path, monkeypatch):
+    digest = "a" * 64
+    rec = {"quant2d_tile_rows": {"bytes_per_launch": 123, "source_sha256": digest}}
+    path = tmp_path / "profiles" / "roofline_traffic.json"
+    path.parent.mkdir()
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda key: digest)
+    assert bench.recorded_traffic("quant2d_tile_rows") == 123
+    rec["quant2d_tile_rows"]["source_sha256"] = "0" * 64      # the kernel changed since
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("quant2d_tile_rows") is None
+    assert bench.recorded_traffic("gemm_mx_kernel") is None      # no record at all
+
+
+def test_every_committed_traffic_record_is_complete():
+    with open(f"{bench.ROOT}/profiles/roofline_traffic.json") as f:
+        recs = json.load(f)
+    assert set(bench.KERNEL_SOURCES) <= set(recs)
+    for key, r in recs.items():
+        assert r["bytes_per_launch"] > 0
+        assert len(r["source_sha256"]) == 64
+        assert "ncu" in r["command"] and "--clock-control none" in r["command"]

@@ -46,12 +46,11 @@ DeviceInfo *current_device() {
 }
 
 bool log_enabled() {
-  static int on = -1;
-  if (on < 0) {
+  static const bool on = [] {   // initialised once, thread-safe
     const char *e = getenv("FP8Q_LOG");
-    on = (e != nullptr && e[0] != '\0' && e[0] != '0') ? 1 : 0;
-  }
-  return on == 1;
+    return e != nullptr && e[0] != '\0' && e[0] != '0';
+  }();
+  return on;
 }
 
 int check_device() {

@@ -432,8 +432,7 @@ template <int STAGES, int ACC, bool OUT_BF16, bool VEC, bool GROUPED>
 int run_tensor_pair(const PairMaps &maps, const PairGroup &grp, cudaStream_t stream) {
   using L = PairLayout<STAGES>;
   auto kernel = gemm_tensor_pair_kernel<STAGES, ACC, OUT_BF16, VEC, GROUPED>;
-  static bool attr_done = false;  // per instantiation
-  static int max_clusters = 0;
+  static PerDeviceOnce setup;  // per instantiation: the pairs that fit at once, 0 on failure
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(192, 1, 1);
@@ -445,14 +444,14 @@ int run_tensor_pair(const PairMaps &maps, const PairGroup &grp, cudaStream_t str
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!attr_done) {
-    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
-    cfg.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg) != cudaSuccess ||
-        max_clusters < 1)
-      return FP8Q_ERR_CUDA;
-    attr_done = true;
-  }
+  const int max_clusters = setup.get([&] {
+    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return 0;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * (sm_count() / 2), 1, 1);
+    int n = 0;
+    return cudaOccupancyMaxActiveClusters(&n, kernel, &q) == cudaSuccess ? n : 0;
+  });
+  if (max_clusters < 1) return FP8Q_ERR_CUDA;
   const int units = grp.unit_end[grp.n - 1];
   if (units <= 0) return FP8Q_OK;
   cfg.gridDim = dim3(2 * (units < max_clusters ? units : max_clusters), 1, 1);
@@ -487,11 +486,9 @@ int run_tensor(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, 
                cudaStream_t stream) {
   using L = Layout<BN, STAGES>;
   auto kernel = gemm_tensor_kernel<BN, STAGES, OUT_BF16, VEC>;
-  static bool attr_done = false;  // per instantiation
-  if (!attr_done) {
-    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
-    attr_done = true;
-  }
+  static PerDeviceOnce setup;  // per instantiation
+  if (setup.get([&] { return set_smem(kernel, L::kSmemBytes) == cudaSuccess ? 1 : 0; }) != 1)
+    return FP8Q_ERR_CUDA;
   kernel<<<grid, 192, L::kSmemBytes, stream>>>(ta, tb, a);
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }

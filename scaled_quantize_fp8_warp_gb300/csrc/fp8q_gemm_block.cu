@@ -359,16 +359,16 @@ int run_blockscaled(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs
   using Cfg = BSConfig<BN, NWG>;
   using L = Layout<BN, Cfg::kStages>;
   auto kernel = gemm_blockscaled_kernel<BN, NWG, B_TILE, OUT_BF16>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static PerDeviceOnce setup;  // per instantiation
+  const int ready = setup.get([&] {
     // The setmaxnreg split is only safe if the kernel launches with at least
     // kLaunchRegs registers per thread; refuse to launch otherwise.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (fa.numRegs < Cfg::kLaunchRegs) return FP8Q_ERR_CUDA;
-    if (set_smem(kernel, L::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
-    attr_done = true;
-  }
+    if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return 0;
+    if (fa.numRegs < Cfg::kLaunchRegs) return 0;
+    return set_smem(kernel, L::kSmemBytes) == cudaSuccess ? 1 : 0;
+  });
+  if (ready != 1) return FP8Q_ERR_CUDA;
   kernel<<<grid, Cfg::kThreads, L::kSmemBytes, stream>>>(ta, tb, a);
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }

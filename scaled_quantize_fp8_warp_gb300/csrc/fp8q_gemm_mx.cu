@@ -204,11 +204,10 @@ template <bool OUT_BF16>
 int run_mx(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &a, int grid,
            cudaStream_t stream) {
   auto kernel = gemm_mx_kernel<OUT_BF16>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (set_smem(kernel, MxLayout::kSmemBytes) != cudaSuccess) return FP8Q_ERR_CUDA;
-    attr_done = true;
-  }
+  static PerDeviceOnce setup;  // per instantiation
+  if (setup.get([&] { return set_smem(kernel, MxLayout::kSmemBytes) == cudaSuccess ? 1 : 0; }) !=
+      1)
+    return FP8Q_ERR_CUDA;
   kernel<<<grid, 320, MxLayout::kSmemBytes, stream>>>(ta, tb, a);
   return cudaGetLastError() == cudaSuccess ? FP8Q_OK : FP8Q_ERR_CUDA;
 }

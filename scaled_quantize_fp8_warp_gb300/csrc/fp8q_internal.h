@@ -5,11 +5,34 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/fp8q.h"
 
 namespace fp8q {
 
 constexpr int kNumSMsHint = 152;
+
+// One-time set-up of a kernel launch (its shared-memory attribute, an
+// occupancy query), run once per device and safe against concurrent first
+// calls: get() runs init() on the first call from the current device and
+// returns that call's result from then on.  Function attributes are
+// per-device state, so a process that drives several devices sets each one.
+class PerDeviceOnce {
+ public:
+  template <typename F>
+  int get(F &&init) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return init();
+    std::call_once(flag_[dev], [&] { value_[dev] = init(); });
+    return value_[dev];
+  }
+
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::once_flag flag_[kMaxDevices];
+  int value_[kMaxDevices] = {};
+};
 
 // Device error word of the current device (set by kernels whose bounded
 // waits expire).  Defined in fp8q_api.cu.

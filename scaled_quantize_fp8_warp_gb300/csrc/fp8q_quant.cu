@@ -1147,16 +1147,18 @@ template <typename InT, int FMT, int KM>
 cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
   using Ring = QuantShape<InT, KM>;
   auto kernel = quant2d_kernel<InT, FMT, KM>;
-  static int blocks_per_sm = 0;
-  if (blocks_per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Ring::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, kQuantThreads,
-                                                      Ring::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (blocks_per_sm < 1) blocks_per_sm = 1;
-  }
+  static PerDeviceOnce setup;  // per instantiation: resident CTAs per SM, 0 on failure
+  const int blocks_per_sm = setup.get([&] {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ring::kSmemBytes) != cudaSuccess)
+      return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kQuantThreads,
+                                                      Ring::kSmemBytes) != cudaSuccess)
+      return 0;
+    return n < 1 ? 1 : n;
+  });
+  if (blocks_per_sm < 1) return cudaErrorInvalidDeviceFunction;
   // The input as a 2D tensor: cols elements per row, rows rows; one box is a
   // 128 x 128 tile, out-of-bounds parts zero-filled.  rows == 0 or cols == 0
   // launches no tile and leaves the map unused.
@@ -1265,18 +1267,18 @@ cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
   unsigned int *out = reinterpret_cast<unsigned int *>(amax);
   unsigned int *err = device_error_word();
   if (err == nullptr) return cudaErrorInvalidValue;
-  static bool attr_done[2] = {false, false};
+  static PerDeviceOnce setup[2];   // bf16, fp32 input
   const int t = in_dtype == FP8Q_DT_BF16 ? 0 : 1;
-  if (!attr_done[t]) {
-    cudaError_t e = t == 0 ? cudaFuncSetAttribute(amax_kernel<uint16_t>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  kAmaxSmem)
-                           : cudaFuncSetAttribute(amax_kernel<float>,
-                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  kAmaxSmem);
-    if (e != cudaSuccess) return e;
-    attr_done[t] = true;
-  }
+  const int ready = setup[t].get([&] {
+    const cudaError_t e = t == 0 ? cudaFuncSetAttribute(amax_kernel<uint16_t>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        kAmaxSmem)
+                                 : cudaFuncSetAttribute(amax_kernel<float>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        kAmaxSmem);
+    return e == cudaSuccess ? 1 : 0;
+  });
+  if (ready != 1) return cudaErrorInvalidDeviceFunction;
   if (in_dtype == FP8Q_DT_BF16)
     amax_kernel<uint16_t><<<(unsigned)blocks, 256, kAmaxSmem, stream>>>(
         static_cast<const uint16_t *>(x), n, out, slot, err);

@@ -42,6 +42,13 @@
  *   - Alignment: every device pointer must be 16-byte aligned
  *     (FP8Q_ERR_MISALIGNED otherwise).  Inner (contiguous) dimensions must be
  *     multiples of 16 where stated (FP8Q_ERR_INVALID_ARG otherwise).
+ *   - Threads and devices: every entry point works on the calling thread's
+ *     current CUDA device and may be called from several host threads at
+ *     once, in a process that drives one device or several; each kernel's
+ *     one-time launch set-up (its shared-memory size attribute, an occupancy
+ *     query) runs once per device.  Work that shares a buffer, an amax
+ *     history or a workspace must be ordered by the caller (one stream, or
+ *     events).
  */
 #ifndef FP8Q_H
 #define FP8Q_H

@@ -871,8 +871,9 @@ def tiny_linear_latency(fq, torch, stream, reps: int = 200):
     """The fp8_parity page's linear (x 512x32, w 64x32, grad_out 512x64, fp32,
     per-tensor current scaling, fp32 outputs): microseconds per call of each
     GEMM (operands quantised beforehand) and of the whole autocast forward +
-    backward (amax, cast with the transposed copy and the three GEMMs), as
-    `reps` back-to-back launches on one stream timed with CUDA events.  At
+    backward (amax and cast with the transposed copy of x, w and grad_out,
+    then the three GEMMs), as `reps` back-to-back calls on one stream timed
+    with CUDA events, and as a replayed CUDA graph of the same calls.  At
     2 MFLOP per GEMM this is launch latency, not a roofline."""
     import workloads
     x, w, g = (t.cuda() for t in workloads.tiny_linear())
@@ -885,6 +886,9 @@ def tiny_linear_latency(fq, torch, stream, reps: int = 200):
     y, dx, dw = e((512, 64), f32), e((512, 32), f32), e((64, 32), f32)
 
     def quantize():
+        # amax, then the cast (two launches per tensor: at these sizes the
+        # one-call form, a memset and a cooperative launch, is no faster
+        # eagerly and slower inside a graph)
         for k in "xwg":
             qq, qt, am, sc = q[k]
             fq.fp8_amax(src[k], out=am, stream=stream)
@@ -917,13 +921,25 @@ def tiny_linear_latency(fq, torch, stream, reps: int = 200):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps * 1e3
 
+    def step():
+        quantize()
+        for fn in gemm.values():
+            fn()
+
     quantize()
     out = {k: round(per_call_us(fn), 2) for k, fn in gemm.items()}
     out["quantize_x_w_g_us"] = round(per_call_us(quantize), 2)
-    out["autocast_fwd_bwd_us"] = round(per_call_us(lambda: (quantize(), [fn() for fn in
-                                                                       gemm.values()])), 2)
+    out["autocast_fwd_bwd_us"] = round(per_call_us(step), 2)
+    # the same nine launches captured once into a CUDA graph and replayed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        out["autocast_fwd_bwd_graph_us"] = round(per_call_us(graph.replay), 2)
     out["note"] = ("us per call, back-to-back on one stream (CUDA events over "
-                   f"{reps} calls); the autocast step is 3 amax + 3 casts + 3 GEMMs = 9 launches")
+                   f"{reps} calls); the autocast step is 3 amax + 3 casts + 3 GEMMs = 9 launches, "
+                   "issued call by call or replayed as one CUDA graph")
     return out
 
 

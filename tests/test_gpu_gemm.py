@@ -113,6 +113,68 @@ def test_tiny_linear_all_roles(fq):
         check_bound(f32(got), yr, ab, False, nm)
 
 
+@pytest.mark.parametrize("one_call", [False, True])
+def test_tiny_linear_replayed_from_a_cuda_graph(fq, one_call):
+    """The tiny linear's autocast step (amax and cast with the transposed copy
+    of x, w and grad_out -- two launches each, or one cooperative launch of
+    fp8_quantize_tensor_current -- then three GEMMs) captured once into a
+    CUDA graph and replayed on new inputs gives the oracle's FP8 bytes and the
+    same outputs, bit for bit, as the same calls made eagerly."""
+    stream = torch.cuda.Stream()
+    bufs = dict(zip("xwg", (t.cuda() for t in workloads.tiny_linear())))
+    fmt = {"x": 0, "w": 0, "g": 1}
+    f32t = torch.float32
+    e = lambda shp, dt: torch.empty(shp, dtype=dt, device="cuda")
+    q = {k: (e(t.shape, torch.uint8), e(t.shape[::-1], torch.uint8), e((1,), f32t),
+             e((1,), f32t)) for k, t in bufs.items()}
+    outs = (e((512, 64), f32t), e((512, 32), f32t), e((64, 32), f32t))
+    T = fq.GemmOperand.tensor
+
+    def step():
+        for k in "xwg":
+            qq, qt, am, sc = q[k]
+            if one_call:
+                fq.fp8_quantize_tensor_current(bufs[k], fmt[k], want_q=True, want_qt=True, q=qq,
+                                               q_t=qt, amax=am, scale=sc, stream=stream)
+            else:
+                fq.fp8_amax(bufs[k], out=am, stream=stream)
+                fq.fp8_quantize_tensor(bufs[k], fmt[k], am, want_q=True, want_qt=True, q=qq,
+                                       q_t=qt, scale=sc, stream=stream)
+        fq.fp8_gemm_fprop(T(q["x"][0], 0, q["x"][3]), T(q["w"][0], 0, q["w"][3]),
+                          out=outs[0], stream=stream)
+        fq.fp8_gemm_dgrad(T(q["g"][0], 1, q["g"][3]), T(q["w"][1], 0, q["w"][3]),
+                          out=outs[1], stream=stream)
+        fq.fp8_gemm_wgrad(T(q["g"][1], 1, q["g"][3]), T(q["x"][1], 0, q["x"][3]),
+                          out=outs[2], stream=stream)
+
+    with torch.cuda.stream(stream):
+        step()   # eager first: each kernel's one-time launch set-up stays outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    for seed in (5, 6):
+        new = dict(zip("xwg", workloads.tiny_linear(seed)))
+        with torch.cuda.stream(stream):
+            for k in "xwg":
+                bufs[k].copy_(new[k].cuda())
+            graph.replay()
+        torch.cuda.synchronize()
+        gpu_status_ok(fq)
+        replayed = [t.clone() for k in "xwg" for t in q[k]] + [o.clone() for o in outs]
+        for k in "xwg":
+            rq, rqt, rs = oracle.quantize_tensor(new[k].numpy(), fmt[k], want_qt=True)
+            assert_bytes_equal(u8(q[k][0]), rq, f"{k} (seed {seed})")
+            assert_bytes_equal(u8(q[k][1]), rqt, f"{k}_t (seed {seed})")
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        eager = [t for k in "xwg" for t in q[k]] + list(outs)
+        for a, b in zip(replayed, eager):
+            assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
 # --------------------------------------- per-tensor, ragged multi-tile shapes
 
 @pytest.mark.parametrize("M,N,K", [(300, 272, 400), (129, 512, 1024), (1000, 1040, 256),

@@ -163,6 +163,25 @@ def test_scale_is_fp32_division():
         assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("fmt", BOTH)
+def test_cast_is_division_near_fp8_midpoints(fmt):
+    """The cast divides (x / scale in fp32, then one rounding into the
+    format); multiplying by a rounded reciprocal is not the definition.
+    Inputs a few ulps around midpoint * s, for every midpoint between
+    neighbouring FP8 magnitudes, put the quotient next to a rounding boundary
+    of the format, where the two differ in a few percent of the cases: the
+    bytes must equal torch's fp32 division followed by its cast."""
+    rng = np.random.default_rng(17)
+    table = oracle.decode_table(fmt)
+    mags = np.unique(np.abs(table[np.isfinite(table)]))
+    mids = (mags[1:] + mags[:-1]) / 2
+    for s in (rng.uniform(0.5, 2, 24) * 2.0 ** rng.integers(-30, 10, 24)).astype(np.float32):
+        x0 = (mids * np.float64(s)).astype(np.float32).view(np.int32)
+        x = np.concatenate([x0 + k for k in range(-3, 4)]).view(np.float32)
+        ref = (torch.from_numpy(x) / torch.tensor(s)).to(FMT[fmt]).view(torch.uint8).numpy()
+        assert np.array_equal(oracle.cast(x, s, fmt), ref)
+
+
 # ------------------------------------------------------ page smoke steps
 
 def _torch_gen(seed):

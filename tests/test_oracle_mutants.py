@@ -98,6 +98,19 @@ MUTANTS = {
     "gemm_abs_sum_signed": (
         "aacc += fabs(a * b);", "aacc += a * b;",
         [("test_gemm_vs_numpy_dense", ("tensor",))]),
+    "tile_cols_scales_column_major": (
+        "scales[(r0 / 128) * cols + c] = s;", "scales[c * ((rows + 127) / 128) + r0 / 128] = s;",
+        [("test_tile_cols_is_rows_of_transpose", (E4,))]),
+    "e5m2_overflow_to_max_instead_of_inf": (
+        "uint8_t ovf_code = (uint8_t)(fmt == ORC_E4M3 ? 0x7F : 0x7C);",
+        "uint8_t ovf_code = (uint8_t)(fmt == ORC_E4M3 ? 0x7F : 0x7B);",
+        [("test_encode_every_bf16_vs_torch", (E5,))]),
+    "delayed_ring_never_advances": (
+        "*next = (*next + 1) % hist_len;", "*next = *next % hist_len;",
+        [("test_delayed_ring_bookkeeping", ())]),
+    "amax_ignores_nan": (
+        "    if (isnan(a)) return a;\n    if (a > m) m = a;", "    if (a > m) m = a;",
+        [("test_amax_brute_force", ())]),
     "mx_emax_off_by_one": (
         "  return ex - 1;\n}", "  return ex;\n}",
         [("test_emax_elem_from_the_page_constants", (E4,)),

@@ -45,13 +45,6 @@ DeviceInfo *current_device() {
   return d;
 }
 
-bool log_enabled() {
-  static const bool on = [] {   // initialised once, thread-safe
-    const char *e = getenv("FP8Q_LOG");
-    return e != nullptr && e[0] != '\0' && e[0] != '0';
-  }();
-  return on;
-}
 
 int check_device() {
   DeviceInfo *d = current_device();
@@ -183,6 +176,14 @@ unsigned int *device_error_word() {
 int sm_count() {
   DeviceInfo *d = current_device();
   return (d && d->sms > 0) ? d->sms : kNumSMsHint;
+}
+
+bool log_enabled() {
+  static const bool on = [] {   // initialised once, thread-safe
+    const char *e = getenv("FP8Q_LOG");
+    return e != nullptr && e[0] != '\0' && e[0] != '0';
+  }();
+  return on;
 }
 
 }  // namespace fp8q

@@ -31,6 +31,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <stdio.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -668,6 +670,19 @@ int launch_gemm(const GemmOperandDev &A, const GemmOperandDev &B, void *C, int o
   }
   int grid = sm_count();
   if (tiles < grid) grid = (int)tiles;
+  if (log_enabled()) {
+    const char *kernel = tensor ? (BN == 256 ? "gemm_tensor_pair_kernel" : "gemm_tensor_kernel")
+                                : (mx ? "gemm_mx_kernel" : "gemm_blockscaled_kernel");
+    const int unit_m = tensor && BN == 256 ? 256 : kBM;
+    fprintf(stderr,
+            "[fp8q] launch %s unit %dx%d units %lld k_blocks %d raster %d%s scales %s out %s\n",
+            kernel, unit_m, BN, (long long)(unit_m == 256 ? (int64_t)((a.num_m_tiles + 1) / 2) *
+                                                                a.num_n_tiles
+                                                          : tiles),
+            a.num_k_blocks, a.group, a.along_n ? " along N" : " along M",
+            vec ? "row" : (tensor ? "tensor" : (mx ? "mx" : "promoted per K block")),
+            bf16 ? "bf16" : "fp32");
+  }
 
   if (tensor) return run_tensor_family(ta, tb, a, grid, BN, bf16, vec, stream);
   if (mx) {
@@ -692,6 +707,8 @@ int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *co
       pair = false;
   }
   if (!pair) {
+    if (log_enabled())
+      fprintf(stderr, "[fp8q] grouped call of %d GEMMs: one launch per GEMM\n", count);
     for (int i = 0; i < count; ++i) {
       const int rc = launch_gemm(A[i], B[i], C[i], out_dtype, M[i], N[i], K[i], stream, nullptr);
       if (rc != FP8Q_OK) return rc;
@@ -714,6 +731,9 @@ int launch_gemm_group(const GemmOperandDev *A, const GemmOperandDev *B, void *co
     raster_for((a.num_m_tiles + 1) / 2, a.num_n_tiles, 256, 256, K[i], a.group, a.along_n);
     add_pair_problem(maps, grp, ta, tb, a);
   }
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] launch gemm_tensor_pair_kernel grouped: %d GEMMs, %lld units 256x256\n",
+            count, (long long)units);
   return run_tensor_pair_group(maps, grp, out_dtype == FP8Q_DT_BF16, stream);
 }
 

@@ -41,6 +41,11 @@ unsigned int *device_error_word();
 // SM count of the current device (cached).
 int sm_count();
 
+// True when the environment sets FP8Q_LOG (to anything but "0"): every entry
+// point and every kernel launch then prints one line to stderr naming what
+// it runs, so a caller can see which kernel served each call.
+bool log_enabled();
+
 // True when M, N, K are non-negative and M*K, N*K (and the byte sums of a
 // linear layer's workspace) fit in int64.  Defined in fp8q_api.cu.
 bool linear_dims_ok(int64_t M, int64_t N, int64_t K);

@@ -36,6 +36,7 @@
 #include <atomic>
 #include <mutex>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include "fp8q_internal.h"
@@ -1182,6 +1183,17 @@ cudaError_t launch_variant(const QuantParams &p, cudaStream_t stream) {
   q.work_slot = (q.dynamic || KM == kKTensorFused)
                     ? (int)(next_slot.fetch_add(1u) % kQuantWorkSlots)
                     : 0;
+  if (log_enabled()) {
+    static const char *const kModeNames[] = {"tensor",   "delayed",  "tile_rows", "tile_cols",
+                                             "tile_both", "block",   "row_amax",  "row_cast",
+                                             "tensor_fused", "mx"};
+    fprintf(stderr,
+            "[fp8q] launch quant2d_kernel mode %s %s input, %lld tiles of 128x128, grid %lld "
+            "(%d per SM)%s%s\n",
+            kModeNames[KM], sizeof(InT) == 2 ? "bf16" : "fp32", (long long)ntiles,
+            (long long)grid, blocks_per_sm, q.dynamic ? ", tiles claimed dynamically" : "",
+            KM == kKTensorFused ? ", cooperative" : "");
+  }
   if (KM == kKTensorFused) {
     // every CTA must be resident for the grid barrier: a cooperative launch
     // guarantees it (or fails)
@@ -1279,6 +1291,9 @@ cudaError_t launch_amax(const void *x, int in_dtype, int64_t n, float *amax,
     return e == cudaSuccess ? 1 : 0;
   });
   if (ready != 1) return cudaErrorInvalidDeviceFunction;
+  if (log_enabled())
+    fprintf(stderr, "[fp8q] launch amax_kernel %s input, %lld elements, grid %lld\n",
+            in_dtype == FP8Q_DT_BF16 ? "bf16" : "fp32", (long long)n, (long long)blocks);
   if (in_dtype == FP8Q_DT_BF16)
     amax_kernel<uint16_t><<<(unsigned)blocks, 256, kAmaxSmem, stream>>>(
         static_cast<const uint16_t *>(x), n, out, slot, err);

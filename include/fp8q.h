@@ -42,6 +42,10 @@
  *   - Alignment: every device pointer must be 16-byte aligned
  *     (FP8Q_ERR_MISALIGNED otherwise).  Inner (contiguous) dimensions must be
  *     multiples of 16 where stated (FP8Q_ERR_INVALID_ARG otherwise).
+ *   - Diagnostics: with the environment variable FP8Q_LOG set (to anything
+ *     but "0") every call and every kernel launch prints one line to stderr
+ *     naming the kernel that serves it, its tile or unit shape and its grid or
+ *     raster.  The variable is read once per process.
  *   - Threads and devices: every entry point works on the calling thread's
  *     current CUDA device and may be called from several host threads at
  *     once, in a process that drives one device or several; each kernel's

@@ -87,3 +87,23 @@ def test_every_committed_traffic_record_is_complete():
         assert r["bytes_per_launch"] > 0
         assert len(r["source_sha256"]) == 64
         assert "ncu" in r["command"] and "--clock-control none" in r["command"]
+
+
+def test_reference_arm_prints_its_line_on_the_host():
+    """`bench.py --impl reference` times the oracle on the host cores and
+    prints one JSON line with the bench contract's keys (one short step)."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=bench.ROOT, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 1 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"]

@@ -73,6 +73,46 @@ class Operand(ctypes.Structure):
                 ("scale_stride_row", ctypes.c_int64), ("scale_stride_k", ctypes.c_int64)]
 
 
+def signatures() -> dict:
+    """ctypes (restype, argtypes) of every entry point, as include/fp8q.h
+    declares them (tests compare the two)."""
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    OP = ctypes.POINTER(Operand)
+    return {
+        "fp8q_status_string": (ctypes.c_char_p, [I32]),
+        "fp8q_device_status": (I32, []),
+        "fp8q_device_supported": (I32, []),
+        "fp8q_selftest_barrier_timeout": (I32, [P]),
+        "fp8_amax": (I32, [P, I32, I64, P, P]),
+        "fp8_quantize_tensor": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+        "fp8_quantize_delayed": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+        "fp8_quantize_tensor_current": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+        "fp8q_history_init": (I32, [P, P, P]),
+        "fp8_quantize_tile1x128": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+        "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
+        "fp8_quantize_block128x128": (I32, [P, I32, I64, I64, I32, P, P, P, I32, P]),
+        "fp8_quantize_mxfp8": (I32, [P, I32, I64, I64, I32, P, P, P, P, P]),
+        "fp8q_mx_scale_bytes": (SZ, [I64, I64]),
+        "fp8_gemm": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+        "fp8_gemm_amax": (I32, [OP, OP, P, I32, I64, I64, I64, P, P]),
+        "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+        "fp8_gemm_dgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+        "fp8_gemm_wgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
+        "fp8_gemm_grouped": (I32, [P, I32, I32, P]),
+        "fp8q_linear_workspace_size": (SZ, [I32, I64, I64, I64]),
+        "fp8_linear_autocast": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32, P, SZ,
+                                      P]),
+        "fp8_linear_autocast_noalloc": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32,
+                                              P]),
+        "fp8q_linear_train_workspace_size": (SZ, [I32, I64, I64, I64]),
+        "fp8_linear_train": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P, I32,
+                                   P, SZ, P]),
+        "fp8q_linear_train_host_workspace_size": (SZ, [I32, I32, I32, I64, I64, I64]),
+        "fp8_linear_train_host": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P,
+                                        I32, P, SZ, P]),
+    }
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -88,41 +128,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 f"{path} not found: build it with `python -m scaled_quantize_fp8_warp_gb300.build_lib`"
                 " (the FP8 path has no fallback)")
         lib = ctypes.CDLL(path)
-        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
-        OP = ctypes.POINTER(Operand)
-        sig = {
-            "fp8q_status_string": (ctypes.c_char_p, [I32]),
-            "fp8q_device_status": (I32, []),
-            "fp8q_device_supported": (I32, []),
-            "fp8q_selftest_barrier_timeout": (I32, [P]),
-            "fp8_amax": (I32, [P, I32, I64, P, P]),
-            "fp8_quantize_tensor": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
-            "fp8_quantize_delayed": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
-            "fp8_quantize_tensor_current": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
-            "fp8q_history_init": (I32, [P, P, P]),
-            "fp8_quantize_tile1x128": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
-            "fp8_quantize_rowwise": (I32, [P, I32, I64, I64, I32, P, P, P, P, I32, P]),
-            "fp8_quantize_block128x128": (I32, [P, I32, I64, I64, I32, P, P, P, I32, P]),
-            "fp8_quantize_mxfp8": (I32, [P, I32, I64, I64, I32, P, P, P, P, P]),
-            "fp8q_mx_scale_bytes": (SZ, [I64, I64]),
-            "fp8_gemm": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
-            "fp8_gemm_amax": (I32, [OP, OP, P, I32, I64, I64, I64, P, P]),
-            "fp8_gemm_fprop": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
-            "fp8_gemm_dgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
-            "fp8_gemm_wgrad": (I32, [OP, OP, P, I32, I64, I64, I64, P]),
-            "fp8_gemm_grouped": (I32, [P, I32, I32, P]),
-            "fp8q_linear_workspace_size": (SZ, [I32, I64, I64, I64]),
-            "fp8_linear_autocast": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32, P, SZ,
-                                          P]),
-            "fp8_linear_autocast_noalloc": (I32, [P, P, I32, I64, I64, I64, I32, P, P, P, I32,
-                                                  P]),
-            "fp8q_linear_train_workspace_size": (SZ, [I32, I64, I64, I64]),
-            "fp8_linear_train": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P, I32,
-                                       P, SZ, P]),
-            "fp8q_linear_train_host_workspace_size": (SZ, [I32, I32, I32, I64, I64, I64]),
-            "fp8_linear_train_host": (I32, [P, P, P, I32, I64, I64, I64, I32, P, P, P, P, P, P,
-                                            I32, P, SZ, P]),
-        }
+        sig = signatures()
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
             fn.restype = res

@@ -303,3 +303,52 @@ def test_product_package_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "fp8_oracle" not in text, f
+
+
+def header_prototypes():
+    """{name: (return type, [parameter types])} of every function include/fp8q.h
+    declares, parameter names dropped."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for ret, name, args in re.findall(
+            r"^\s*((?:const\s+)?[A-Za-z_0-9]+\s*\*?)\s*([a-z_0-9]+)\s*\(([^;{]*?)\)\s*;",
+            text, flags=re.M | re.S):
+        params = []
+        for a in args.replace("\n", " ").split(","):
+            a = re.sub(r"\s+", " ", a).strip()
+            if a and a != "void":
+                params.append(re.sub(r"\s*[A-Za-z_0-9]+$", "", a).strip())   # drop the name
+        out[name] = (re.sub(r"\s+", " ", ret).strip(), params)
+    return out
+
+
+def _ctype_class(t: str) -> str:
+    """The ctypes class a C parameter or return type needs."""
+    t = t.replace("const ", "")
+    if t == "char *":
+        return "char_p"
+    if t.endswith("*") or t == "cudaStream_t":
+        return "pointer"
+    return {"int": "i32", "int32_t": "i32", "int64_t": "i64", "size_t": "size"}[t]
+
+
+def _ctypes_class(ct) -> str:
+    import scaled_quantize_fp8_warp_gb300 as fq
+    if ct is ctypes.c_char_p:
+        return "char_p"
+    if ct is ctypes.c_void_p or ct is ctypes.POINTER(fq.Operand):
+        return "pointer"
+    return {ctypes.c_int: "i32", ctypes.c_int64: "i64", ctypes.c_size_t: "size"}[ct]
+
+
+def test_binding_signatures_match_the_header():
+    """Every argument the binding marshals has the width and kind the header
+    declares (a missing or mis-sized argument would be undefined behaviour)."""
+    import scaled_quantize_fp8_warp_gb300 as fq
+    protos = header_prototypes()
+    sigs = fq.signatures()
+    assert sorted(protos) == sorted(sigs)
+    for name, (ret, params) in protos.items():
+        res, args = sigs[name]
+        assert _ctype_class(ret) == _ctypes_class(res), name
+        assert [_ctype_class(p) for p in params] == [_ctypes_class(a) for a in args], name

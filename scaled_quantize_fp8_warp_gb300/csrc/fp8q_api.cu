@@ -63,6 +63,8 @@ int check_quant(const void *x, int in_dtype, int64_t rows, int64_t cols, int for
                 bool want_t) {
   if (!valid_dtype(in_dtype) || !valid_format(format)) return FP8Q_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0) return FP8Q_ERR_INVALID_ARG;
+  // the byte size of x (4-byte elements at most) must fit in int64
+  if (rows > 0 && cols > INT64_MAX / 4 / rows) return FP8Q_ERR_INVALID_ARG;
   if (cols % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   if (want_t && rows % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   if (rows > 0 && cols > 0) {
@@ -235,7 +237,8 @@ int fp8q_selftest_barrier_timeout(cudaStream_t stream) {
 }
 
 int fp8_amax(const void *x, int in_dtype, int64_t n, float *amax, cudaStream_t stream) {
-  if (!valid_dtype(in_dtype) || n < 0 || amax == nullptr) return FP8Q_ERR_INVALID_ARG;
+  if (!valid_dtype(in_dtype) || n < 0 || n > INT64_MAX / 4 || amax == nullptr)
+    return FP8Q_ERR_INVALID_ARG;
   if (n > 0 && x == nullptr) return FP8Q_ERR_INVALID_ARG;
   if (n > 0 && !aligned16(x)) return FP8Q_ERR_MISALIGNED;
   if ((reinterpret_cast<uintptr_t>(amax) & 3u) != 0) return FP8Q_ERR_MISALIGNED;
@@ -499,6 +502,10 @@ namespace {
 int gemm_common(const fp8q_operand *A, const fp8q_operand *B, void *C, int out_dtype, int64_t M,
                 int64_t N, int64_t K, float *amax_out, cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 0 || !valid_dtype(out_dtype)) return FP8Q_ERR_INVALID_ARG;
+  // operand bytes M K and N K, and output bytes (4 per element at most), fit in int64
+  if ((M > 0 && K > INT64_MAX / M) || (N > 0 && K > INT64_MAX / N) ||
+      (M > 0 && N > INT64_MAX / 4 / M))
+    return FP8Q_ERR_INVALID_ARG;
   if (N % 16 != 0 || K % 16 != 0) return FP8Q_ERR_INVALID_ARG;
   int rc;
   if ((rc = check_operand(A, M, K)) != FP8Q_OK) return rc;

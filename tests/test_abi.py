@@ -135,6 +135,17 @@ def test_validation_before_device(lib):
                              32, P(0x10002), None) == 2
     assert lib.fp8_gemm_amax(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 24,
                              32, aligned, None) == 1
+    # sizes whose byte counts overflow int64 are rejected before any arithmetic on them
+    big = 1 << 40
+    assert lib.fp8_quantize_tensor(aligned, fq.DT_BF16, big, big, fq.E4M3, aligned, None,
+                                   aligned, None, 0, None) == 1
+    assert lib.fp8_quantize_tile1x128(aligned, fq.DT_F32, big, big, fq.E4M3, aligned, aligned,
+                                      None, None, 0, None) == 1
+    assert lib.fp8_amax(aligned, fq.DT_F32, 1 << 62, aligned, None) == 1
+    assert lib.fp8_gemm(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, big, big, 32,
+                        None) == 1
+    assert lib.fp8_gemm(ctypes.byref(op), ctypes.byref(op), aligned, fq.DT_BF16, 32, 32,
+                        1 << 60, None) == 1
     # autocast: workspace too small
     assert lib.fp8_linear_autocast(aligned, aligned, fq.DT_BF16, 32, 32, 32, 0, None, None,
                                    aligned, fq.DT_BF16, aligned, 16, None) == 4

@@ -71,7 +71,8 @@ extern "C" {
 typedef enum fp8q_status {
   FP8Q_OK = 0,
   FP8Q_ERR_INVALID_ARG = 1,     /* null where required, negative size, bad enum,
-                                   inner dimension not a multiple of 16 */
+                                   inner dimension not a multiple of 16, sizes
+                                   whose byte counts do not fit in int64 */
   FP8Q_ERR_MISALIGNED = 2,      /* a device pointer is not 16-byte aligned */
   FP8Q_ERR_ARCH = 3,            /* current device is not compute capability 10.3 */
   FP8Q_ERR_WORKSPACE = 4,       /* workspace missing or smaller than required */

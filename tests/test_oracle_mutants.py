@@ -111,6 +111,22 @@ MUTANTS = {
     "amax_ignores_nan": (
         "    if (isnan(a)) return a;\n    if (a > m) m = a;", "    if (a > m) m = a;",
         [("test_amax_brute_force", ())]),
+    "tensor_transposed_copy_in_row_layout": (
+        "      if (q) q[r * cols + c] = b;\n      if (q_t) q_t[c * rows + r] = b;",
+        "      if (q) q[r * cols + c] = b;\n      if (q_t) q_t[r * cols + c] = b;",
+        [("test_tensor_matches_page_and_transpose", (E4,))]),
+    "e5m2_inf_decoded_as_nan": (
+        "v = (m == 0) ? INFINITY : NAN;", "v = NAN;",
+        [("test_decode_all_bytes_vs_torch", (E5,))]),
+    "saturate_flag_ignored": (
+        "(saturate ? max_code : ovf_code)", "(ovf_code)",
+        [("test_encode_saturating", (E4,)), ("test_encode_saturating", (E5,))]),
+    "gemm_sums_magnitudes": (
+        "    acc += a * b;\n", "    acc += fabs(a * b);\n",
+        [("test_gemm_vs_numpy_dense", ("tensor",))]),
+    "mx_exponent_not_clamped_below": (
+        "    if (e < -127) e = -127;\n", "",
+        [("test_mx_scale_special_cases", ()), ("test_mx_scale_bracket_in_exact_rationals", (E4,))]),
     "mx_emax_off_by_one": (
         "  return ex - 1;\n}", "  return ex;\n}",
         [("test_emax_elem_from_the_page_constants", (E4,)),

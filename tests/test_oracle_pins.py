@@ -601,6 +601,10 @@ def test_mx_scale_special_cases():
         fm = oracle.fmax(fmt)
         for k in (-20, -3, 0, 5, 40):
             assert oracle.mx_scale_code(fm * 2.0 ** k, fmt) == 127 + k
+        # a block max so small that floor(log2 amax) - emax_elem falls below E8M0's
+        # -127 takes the clamped exponent -127 (code 0), as an all-zero block does
+        for tiny in (2.0 ** -120, 2.0 ** -140, 2.0 ** -149):
+            assert oracle.mx_scale_code(tiny, fmt) == 0
 
 
 def _nearest_code_brute(v: Fraction, fmt: int) -> int:

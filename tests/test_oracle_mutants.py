@@ -181,3 +181,18 @@ def test_pins_catch_the_planted_mistake(name, tmp_path, monkeypatch):
     _use(monkeypatch, _compile(tmp_path, name, old, new))
     survived = [(p, a) for p, a in cases if not _fails(p, a)]
     assert survived == [], f"{name} passes {survived}"
+
+
+@pytest.mark.parametrize("bits", [7, 9])
+def test_bf16_spacing_pin_catches_a_wrong_significand_width(bits, monkeypatch):
+    """The GEMM bound's bf16 allowance lives in the Python wrapper: plant a
+    spacing for a significand of the wrong width there instead."""
+    import numpy as np
+
+    def wrong(v):
+        a = np.abs(np.asarray(v, dtype=np.float64))
+        e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+        return np.ldexp(1.0, (e - (bits - 1)).astype(np.int64))
+
+    monkeypatch.setattr(oracle, "bf16_ulp", wrong)
+    assert _fails("test_bf16_ulp_vs_torch_spacing", ())

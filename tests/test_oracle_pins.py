@@ -469,6 +469,22 @@ def test_gemm_transpose_symmetry():
     assert np.allclose(y1, y2.T, rtol=1e-14, atol=0)
 
 
+def test_bf16_ulp_vs_torch_spacing():
+    """The bf16 output allowance of the GEMM bound is one bf16 spacing at the
+    reference value: the gap from a bf16 number to the next one up, taken
+    from torch's bf16 bit patterns, over normal magnitudes of both signs."""
+    rng = np.random.default_rng(24)
+    v = (rng.standard_normal(5000) * 2.0 ** rng.integers(-100, 100, 5000)).astype(np.float32)
+    t = torch.from_numpy(v).to(torch.bfloat16)
+    a = t.abs()
+    up = (a.view(torch.int16) + 1).view(torch.bfloat16)
+    spacing = (up.double() - a.double()).numpy()
+    assert np.array_equal(oracle.bf16_ulp(t.double().numpy()), spacing)
+    # and rounding any value to bf16 moves it by at most half of that spacing
+    assert np.all(np.abs(t.double().numpy() - v.astype(np.float64))
+                  <= oracle.bf16_ulp(v.astype(np.float64)) / 2)
+
+
 def test_fp8matmul_roles_vs_page_torch():
     """Fprop / Dgrad / Wgrad on the tiny linear match the page's FP8Matmul
     (forward xq @ wq.T, backward gq @ wq and gq.T @ xq, fp32 on dequantised

@@ -196,7 +196,7 @@ int fp8_quantize_tensor_current(const void *x, int in_dtype, int64_t rows,
                                 int saturate, cudaStream_t stream);
 
 /* Per-tensor delayed scaling ([fp8_parity] smoke step 3; [te_blog]
- * DelayedScaling "relies on an amax history"): s = max(fl32(max(hist->amax) /
+ * DelayedScaling, which keeps a history of amax values): s = max(fl32(max(hist->amax) /
  * fmax), 1e-12) is computed from the history alone, x is cast with s, then
  * amax(x) -- found in the same pass over x -- overwrites hist->amax[hist->next]
  * and hist->next advances modulo FP8Q_HISTORY_LEN.  hist->scale receives s.
@@ -367,8 +367,8 @@ int fp8_gemm_amax(const fp8q_operand *A, const fp8q_operand *B, void *C,
                   float *amax_out, cudaStream_t stream);
 
 /* The three GEMMs of a linear layer y = x w^T with x [M, K] (tokens x input
- * features), w [N, K], grad_out g [M, N] ([fp8_parity] FP8Matmul; [te_blog]
- * "Fprop, Dgrad, and Wgrad shapes are all benchmarked individually").  M, N, K
+ * features), w [N, K], grad_out g [M, N] ([fp8_parity] FP8Matmul; [te_blog],
+ * which times the Fprop, Dgrad and Wgrad shapes one by one).  M, N, K
  * are always the LAYER's sizes; each call maps them onto fp8_gemm:
  *   fprop: y [M, N]  = x [M, K] . w [N, K]^T        (contraction K)
  *   dgrad: dx [M, K] = g [M, N] . w                 (contraction N;
@@ -423,8 +423,8 @@ int fp8_gemm_grouped(const fp8q_gemm_desc *descs, int count, int out_dtype,
  * reject with FP8Q_ERR_INVALID_ARG). */
 size_t fp8q_linear_workspace_size(int recipe, int64_t M, int64_t N, int64_t K);
 
-/* Autocast forward of a linear layer ([te_blog] "autocast mode": inputs are
- * quantized dynamically before each GEMM, and the time covers both): with
+/* Autocast forward of a linear layer ([te_blog] autocast mode: the inputs are
+ * quantised on the fly ahead of every GEMM and the timing includes that): with
  * x [M, K] and w [N, K] in in_dtype, quantizes both to E4M3 under `recipe`
  * and computes y [M, N] = x w^T in out_dtype, all on `stream`, without
  * synchronising.
@@ -452,8 +452,8 @@ size_t fp8q_linear_train_workspace_size(int recipe, int64_t M, int64_t N, int64_
 /* The three GEMMs of one linear layer in training, each operand quantized
  * on the fly ([fp8_parity] FP8Matmul: the forward quantizes x and w to E4M3
  * and returns xq @ wq.T; the backward quantizes grad_out to E5M2 and returns
- * gq @ wq and gq.T @ xq; [te_blog] "autocast mode": inputs are quantized
- * dynamically before each GEMM):
+ * gq @ wq and gq.T @ xq; [te_blog] autocast mode: the inputs are quantised
+ * on the fly ahead of every GEMM):
  *   y  [M, N] = x [M, K] . w [N, K]^T      (Fprop)
  *   dx [M, K] = g [M, N] . w               (Dgrad)
  *   dw [N, K] = g^T . x                    (Wgrad)

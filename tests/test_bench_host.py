@@ -128,3 +128,32 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+def test_profile_summaries_name_runnable_cases():
+    """Every ncu summary under profiles/ gives a command that runs committed
+    files only: each `--profile-case` it names exists in bench.py (templates
+    such as layer_<recipe>_<linear> expand to existing cases), and every ncu
+    command leaves the clocks alone."""
+    import glob
+    import itertools
+    import os
+    import re
+    paths = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.md")) +
+                   glob.glob(os.path.join(bench.ROOT, "profiles", "*.json")))
+    assert paths
+    fill = {"<recipe>": ("tensor", "block", "mx"),
+            "<linear>": ("qkv", "attn_out", "mlp_up", "mlp_down")}
+    for path in paths:
+        text = open(path).read()
+        for case in re.findall(r"--profile-case ([a-z_<>]+)", text):
+            slots = [s for s in fill if s in case]
+            for combo in itertools.product(*(fill[s] for s in slots)):
+                name = case
+                for s, v in zip(slots, combo):
+                    name = name.replace(s, v)
+                assert name in bench.PROFILE_CASES, (os.path.basename(path), name)
+        for cmd in re.findall(r"ncu [^\n]*", text):
+            if "--metrics" in cmd or "--set" in cmd or "--section" in cmd:
+                block = text[text.index(cmd):text.index(cmd) + 400]
+                assert "--clock-control none" in block, (os.path.basename(path), cmd)

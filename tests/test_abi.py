@@ -363,3 +363,56 @@ def test_binding_signatures_match_the_header():
         res, args = sigs[name]
         assert _ctype_class(ret) == _ctypes_class(res), name
         assert [_ctype_class(p) for p in params] == [_ctypes_class(a) for a in args], name
+
+
+@pytest.mark.skipif(_has_cuda_device(),
+                    reason="valid combinations would reach a kernel launch on placeholder pointers")
+def test_random_arguments_get_a_status_not_a_crash(lib):
+    """Seeded random arguments (sizes negative, zero, odd, huge; bad enums;
+    null, aligned or misaligned placeholder pointers) to the quantize, amax
+    and GEMM entry points: every call returns a documented status and none
+    touches memory before its checks.  Here no device exists, so arguments
+    that pass validation stop at the device check (ARCH 3 or CUDA 6)."""
+    import random
+    import scaled_quantize_fp8_warp_gb300 as fq
+    rng = random.Random(1234)
+    P = ctypes.c_void_p
+    sizes = [-1, 0, 1, 15, 16, 17, 128, 130, 4096, 1 << 31, 1 << 40, (1 << 62) + 16]
+    ptrs = [None, P(0x10000), P(0x10008), P(0x10004)]
+    dts = [fq.DT_F32, fq.DT_BF16, 2, -1]
+    fmts = [fq.E4M3, fq.E5M2, 2, -1]
+    scalings = [fq.SCALE_TENSOR, fq.SCALE_TILE_1x128, fq.SCALE_BLOCK_128x128, fq.SCALE_ROW,
+                fq.SCALE_MX_1x32, 5, -1]
+    documented = {1, 2, 3, 6, 7}
+    pick = rng.choice
+    for _ in range(3000):
+        kind = rng.randrange(6)
+        if kind == 0:
+            rc = lib.fp8_amax(pick(ptrs), pick(dts), pick(sizes), pick(ptrs), None)
+        elif kind == 1:
+            rc = lib.fp8_quantize_tensor(pick(ptrs), pick(dts), pick(sizes), pick(sizes),
+                                         pick(fmts), pick(ptrs), pick(ptrs), pick(ptrs),
+                                         pick(ptrs), rng.randrange(2), None)
+        elif kind == 2:
+            rc = lib.fp8_quantize_tile1x128(pick(ptrs), pick(dts), pick(sizes), pick(sizes),
+                                            pick(fmts), pick(ptrs), pick(ptrs), pick(ptrs),
+                                            pick(ptrs), rng.randrange(2), None)
+        elif kind == 3:
+            rc = lib.fp8_quantize_block128x128(pick(ptrs), pick(dts), pick(sizes), pick(sizes),
+                                               pick(fmts), pick(ptrs), pick(ptrs), pick(ptrs),
+                                               rng.randrange(2), None)
+        elif kind == 4:
+            rc = lib.fp8_quantize_mxfp8(pick(ptrs), pick(dts), pick(sizes), pick(sizes),
+                                        pick(fmts), pick(ptrs), pick(ptrs), pick(ptrs),
+                                        pick(ptrs), None)
+        else:
+            def operand():
+                d, s = pick(ptrs), pick(ptrs)
+                return fq.Operand(d.value if d is not None else None, pick(fmts), pick(scalings),
+                                  s.value if s is not None else None, pick(sizes[:6]),
+                                  pick(sizes[:6]))
+            a, b = operand(), operand()
+            fn = pick([lib.fp8_gemm, lib.fp8_gemm_fprop, lib.fp8_gemm_dgrad, lib.fp8_gemm_wgrad])
+            rc = fn(ctypes.byref(a), ctypes.byref(b), pick(ptrs), pick(dts), pick(sizes),
+                    pick(sizes), pick(sizes), None)
+        assert rc in documented, (kind, rc)
